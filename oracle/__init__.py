@@ -1,0 +1,376 @@
+"""fp64 CPU oracle for speculative-decoding verification attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  The CUDA library never imports,
+links or calls it, and it shares no code with the CUDA sources.
+
+The attention, the log-sum-exp merge and the tree visibility are evaluated by
+``verify_oracle.c`` (plain C, fp64, OpenMP over rows).  This module builds that
+file with gcc, widens nothing itself, and assembles for each sequence the
+explicit key list and the explicit full visibility matrix the C code consumes:
+
+* dense   (LongSpec 2.C "Hybrid Tree Attention"): keys are cache rows
+  0 .. L_b+T-1; prefix rows are visible to every draft token (the cache part
+  carries no mask), draft rows L_b+j are visible per the draft bitmask.
+* paged   (HiSpec 2, "batched inference" with paged attention and block
+  tables): the page table is resolved into a separate contiguous copy of the
+  sequence first, then treated as dense.
+* sparse  (Dustin 1 and 3, verification over a fixed-size set I_verify): the
+  prefix keys are the cache rows listed in the verify set of that kv-head,
+  followed by the draft rows.
+
+The verify-set selection (Dustin 1, "hybrid attention aggregation") is here
+too, written as a full stable sort of candidates by (score descending, index
+ascending).
+
+Readings where the pages are silent are documented with each function.
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "verify_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16, F32, F64 = 0, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile verify_oracle.c into a shared library (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_masked_attention.restype = ctypes.c_int
+            lib.oracle_masked_attention.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_longlong,
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_lse_merge.restype = None
+            lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_longlong, ctypes.c_int,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_tree_visibility.restype = ctypes.c_int
+            lib.oracle_tree_visibility.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+@contextlib.contextmanager
+def swapped_library(path: str):
+    """Test hook: run every wrapper below against another build of verify_oracle.c
+    (the mutation tests compile deliberately broken copies to show the pins catch them)."""
+    global _lib
+    _load()
+    saved = _lib
+    try:
+        with _lock:
+            _lib = None
+        lib = ctypes.CDLL(path)
+        for name in ("oracle_masked_attention", "oracle_lse_merge", "oracle_tree_visibility",
+                     "oracle_num_threads", "oracle_set_num_threads"):
+            f, g = getattr(lib, name), getattr(saved, name)
+            f.restype, f.argtypes = g.restype, g.argtypes
+        _lib = lib
+        yield
+    finally:
+        _lib = saved
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def _code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16  # raw bfloat16 bit patterns
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"unsupported array dtype {a.dtype}")
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# ----------------------------------------------------------------------------
+# primitives (C)
+# ----------------------------------------------------------------------------
+
+def masked_attention(q, k, v, visible, scale):
+    """Masked softmax attention of one sequence over an explicit key list.
+
+    q [T][Hq][D]; k, v [n][Hkv][D]; visible bool [T][n].  Arrays are float64,
+    float32 or uint16 (bf16 bits).  Returns out f64 [T][Hq][D], lse f64 [Hq][T].
+    """
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    T, Hq, D = q.shape
+    n, Hkv, Dk = k.shape
+    assert Dk == D and v.shape == k.shape and k.dtype == v.dtype
+    vis = np.ascontiguousarray(visible, dtype=np.uint8)
+    assert vis.shape == (T, n)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    lse = np.zeros((Hq, T), dtype=np.float64)
+    rc = _load().oracle_masked_attention(T, Hq, Hkv, D, float(scale), n, _ptr(q), _code(q), _ptr(k), _ptr(v),
+                                         _code(k), _ptr(vis), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_masked_attention rejected its arguments")
+    return out, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Exact log-sum-exp merge of partial attentions (LongSpec 2.C, LSE fusion).
+
+    o_parts f64 [S][R][D], lse_parts f64 [S][R] -> out f64 [R][D], lse f64 [R].
+    """
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    S, R, D = o_parts.shape
+    out = np.zeros((R, D), dtype=np.float64)
+    lse = np.zeros(R, dtype=np.float64)
+    _load().oracle_lse_merge(S, R, D, _ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def tree_visibility(parent):
+    """Ancestor-or-self visibility bool [T][T] of a parent-pointer tree (LongSpec 1.3, 2.C)."""
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    T = parent.shape[0]
+    vis = np.zeros((T, T), dtype=np.uint8)
+    if _load().oracle_tree_visibility(T, _ptr(parent), _ptr(vis)) != 0:
+        raise ValueError("parent array is not a topologically ordered forest")
+    return vis.astype(bool)
+
+
+# ----------------------------------------------------------------------------
+# bitmask words <-> boolean rows (the draft-mask layout of the library's ABI)
+# ----------------------------------------------------------------------------
+
+def words_to_bool(words, T):
+    """uint32 words [..., W] -> bool [..., T]; bit j % 32 of word j // 32 is token j."""
+    words = np.asarray(words, dtype=np.uint32)
+    out = np.zeros(words.shape[:-1] + (T,), dtype=bool)
+    for j in range(T):
+        out[..., j] = (words[..., j // 32] >> np.uint32(j % 32)) & np.uint32(1) == 1
+    return out
+
+
+def bool_to_words(rows):
+    rows = np.asarray(rows, dtype=bool)
+    T = rows.shape[-1]
+    W = (T + 31) // 32
+    out = np.zeros(rows.shape[:-1] + (W,), dtype=np.uint32)
+    for j in range(T):
+        out[..., j // 32] |= rows[..., j].astype(np.uint32) << np.uint32(j % 32)
+    return out
+
+
+def tree_mask_words(parent):
+    """Per-sequence ancestor bitmask words uint32 [B][T][ceil(T/32)] from parent int32 [B][T]."""
+    parent = np.asarray(parent, dtype=np.int32)
+    return np.stack([bool_to_words(tree_visibility(p)) for p in parent])
+
+
+# ----------------------------------------------------------------------------
+# verification attention per layout
+# ----------------------------------------------------------------------------
+
+def _draft_visibility(draft_vis_b, n_prefix_cols, T):
+    """Explicit [T][n_prefix + T] matrix: prefix columns all visible, draft columns per mask."""
+    vis = np.zeros((T, n_prefix_cols + T), dtype=bool)
+    vis[:, :n_prefix_cols] = True
+    vis[:, n_prefix_cols:] = draft_vis_b
+    return vis
+
+
+def attention_dense(q, k_cache, v_cache, seqlens, draft_vis, scale):
+    """Dense layout.  q [B][T][Hq][D]; caches [B][Lmax][Hkv][D] with the draft
+    keys already at slots L_b .. L_b+T-1; draft_vis bool [B][T][T].
+    Returns out f64 [B][T][Hq][D], lse f64 [B][Hq][T]."""
+    B, T, Hq, D = q.shape
+    out = np.zeros((B, T, Hq, D))
+    lse = np.zeros((B, Hq, T))
+    for b in range(B):
+        L = int(seqlens[b])
+        vis = _draft_visibility(draft_vis[b], L, T)
+        out[b], lse[b] = masked_attention(q[b], k_cache[b, : L + T], v_cache[b, : L + T], vis, scale)
+    return out, lse
+
+
+def gather_pages(pages, page_table_b, n_tokens, page_size):
+    """Contiguous copy [n_tokens][Hkv][D] of one sequence held in pages [P][page][Hkv][D]."""
+    pos = np.arange(n_tokens)
+    page = np.asarray(page_table_b)[pos // page_size]
+    if np.any(page < 0) or np.any(page >= pages.shape[0]):
+        raise ValueError("page table entry out of range")
+    return pages[page, pos % page_size]
+
+
+def attention_paged(q, k_pages, v_pages, page_table, page_size, seqlens, draft_vis, scale):
+    """Paged layout: resolve each sequence's pages into a separate contiguous copy, then dense."""
+    B, T, Hq, D = q.shape
+    out = np.zeros((B, T, Hq, D))
+    lse = np.zeros((B, Hq, T))
+    for b in range(B):
+        L = int(seqlens[b])
+        k = gather_pages(k_pages, page_table[b], L + T, page_size)
+        v = gather_pages(v_pages, page_table[b], L + T, page_size)
+        vis = _draft_visibility(draft_vis[b], L, T)
+        out[b], lse[b] = masked_attention(q[b], k, v, vis, scale)
+    return out, lse
+
+
+def attention_sparse(q, k_cache, v_cache, seqlens, indices, n_indices, draft_vis, scale):
+    """Sparse layout: per (b, kv-head) the prefix keys are rows indices[b][h][:n] of
+    the full cache (no compaction of the cache itself), then the T draft rows."""
+    B, T, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    g = Hq // Hkv
+    out = np.zeros((B, T, Hq, D))
+    lse = np.zeros((B, Hq, T))
+    for b in range(B):
+        L = int(seqlens[b])
+        for h in range(Hkv):
+            n = int(n_indices[b][h])
+            idx = np.asarray(indices[b][h][:n], dtype=np.int64)
+            if np.any(idx < 0) or np.any(idx >= L):
+                raise ValueError("verify index out of range")
+            rows = np.concatenate([idx, np.arange(L, L + T)])
+            k = k_cache[b][rows][:, h: h + 1]
+            v = v_cache[b][rows][:, h: h + 1]
+            vis = _draft_visibility(draft_vis[b], n, T)
+            o, l = masked_attention(q[b][:, h * g:(h + 1) * g], k, v, vis, scale)
+            out[b][:, h * g:(h + 1) * g] = o
+            lse[b][h * g:(h + 1) * g] = l
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# verify index set (Dustin section 1)
+# ----------------------------------------------------------------------------
+
+def _top_by_score(cand, score, count):
+    """The ``count`` candidates with the largest score; equal scores go to the lower index."""
+    if count <= 0 or len(cand) == 0:
+        return cand[:0]
+    order = np.lexsort((cand, -score[cand]))  # primary key: score descending; then index ascending
+    return cand[order[:count]]
+
+
+def build_verify_index(score_draft, score_target, seqlens, n_sink, window, m_draft, budget):
+    """Fixed-size verify set per (sequence, kv-head).
+
+    I = sinks {0..n_sink-1}  U  recent window {L-window .. L-1}
+        U  top-m_draft of score_draft among the other positions
+        U  top of score_target among those still unchosen, filling up to budget,
+    clipped to [0, L) and sorted ascending; |I| = min(budget, L).
+    score_* fp32 [B][Hkv][>=L]; returns idx int32 [B][Hkv][budget] (tail -1), n int32 [B][Hkv].
+    Requires budget >= n_sink + window; scores must not be NaN.
+    """
+    if budget < n_sink + window:
+        raise ValueError("budget smaller than sinks + window")
+    B, Hkv = score_draft.shape[:2]
+    idx = np.full((B, Hkv, budget), -1, dtype=np.int32)
+    cnt = np.zeros((B, Hkv), dtype=np.int32)
+    for b in range(B):
+        L = int(seqlens[b])
+        fixed = np.zeros(L, dtype=bool)
+        fixed[: min(n_sink, L)] = True
+        fixed[max(0, L - window):] = True
+        cand = np.nonzero(~fixed)[0]
+        room = budget - int(fixed.sum())
+        for h in range(Hkv):
+            sd = np.asarray(score_draft[b, h, :L], dtype=np.float32)
+            st = np.asarray(score_target[b, h, :L], dtype=np.float32)
+            pick_d = _top_by_score(cand, sd, min(m_draft, room))
+            rest = np.setdiff1d(cand, pick_d, assume_unique=True)
+            pick_t = _top_by_score(rest, st, room - len(pick_d))
+            sel = np.concatenate([np.nonzero(fixed)[0], pick_d, pick_t])
+            sel = np.sort(sel)
+            cnt[b, h] = len(sel)
+            idx[b, h, : len(sel)] = sel
+    return idx, cnt
+
+
+# ----------------------------------------------------------------------------
+# whole verification step for a workload object (duck-typed)
+# ----------------------------------------------------------------------------
+
+def _host_array(t):
+    """numpy view of a CPU tensor: bf16 -> uint16 bits, fp32 -> float32 (no arithmetic)."""
+    import torch  # local: only for reading tensors handed in by the tests
+
+    if isinstance(t, np.ndarray):
+        return t
+    t = t.detach().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    if t.dtype == torch.float64:
+        return t.numpy()
+    raise TypeError(t.dtype)
+
+
+def draft_visibility(w):
+    """bool [B][T][T]: ancestor-or-self from parents when the workload has a tree,
+    else its explicit bitmask words."""
+    if w.parent is not None:
+        return np.stack([tree_visibility(p) for p in w.parent])
+    return words_to_bool(w.mask_words, w.T)
+
+
+def verify(w, indices=None, n_indices=None):
+    """Reference output of one verification step for workload ``w``.
+
+    Returns dict(out f64 [B][T][Hq][D], lse f64 [B][Hq][T], mask_words, and for
+    the sparse layout indices/n_indices).
+    """
+    vis = draft_visibility(w)
+    q = _host_array(w.q)
+    res = {"mask_words": bool_to_words(vis)}
+    if w.layout == "dense":
+        res["out"], res["lse"] = attention_dense(q, _host_array(w.k_cache), _host_array(w.v_cache),
+                                                 w.seqlens, vis, w.scale)
+    elif w.layout == "paged":
+        res["out"], res["lse"] = attention_paged(q, _host_array(w.k_pages), _host_array(w.v_pages),
+                                                 w.page_table, w.page_size, w.seqlens, vis, w.scale)
+    elif w.layout == "sparse":
+        if indices is None:
+            indices, n_indices = build_verify_index(w.score_draft, w.score_target, w.seqlens, w.n_sink,
+                                                    w.window, w.m_draft, w.budget)
+        res["indices"], res["n_indices"] = indices, n_indices
+        res["out"], res["lse"] = attention_sparse(q, _host_array(w.k_cache), _host_array(w.v_cache),
+                                                  w.seqlens, indices, n_indices, vis, w.scale)
+    else:
+        raise ValueError(w.layout)
+    return res

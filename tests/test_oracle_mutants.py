@@ -1,0 +1,95 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies oracle/verify_oracle.c, plants one mistake (a dropped term, a
+wrong sign, index or operand), builds the copy with gcc and checks that the pin
+set used in test_oracle_pins.py rejects it, while the pristine source passes.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from oracle import twin
+from tests.test_oracle_pins import _f64, _rand_case, _sdpa, _prefix_tree_split
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "verify_oracle.c")
+
+MUTANTS = {
+    "gqa_mapping": ("const int kvh = h / group;", "const int kvh = h % Hkv;"),
+    "dropped_scale": ("z[n] = scale * s;", "z[n] = s;"),
+    "lse_without_max": ("const double l = zmax + log(sum);", "const double l = log(sum);"),
+    "mask_ignored_in_pv": ("if (!vis[n]) continue;\n          const double p", "const double p"),
+    "transposed_q_index": ("s += widen(q, q_dtype, ((size_t)i * Hq + h) * D + d)",
+                           "s += widen(q, q_dtype, ((size_t)h * T + i) * D + d)"),
+    "bf16_widening_shift": ("<< 16;", "<< 15;"),
+    "merge_weight_sign": ("const double w = exp(lse_parts[(size_t)s * n_rows + r] - l);",
+                          "const double w = exp(l - lse_parts[(size_t)s * n_rows + r]);"),
+    "merge_drops_a_part": ("for (int s = 0; s < n_parts; ++s) {\n      const double w",
+                           "for (int s = 1; s < n_parts; ++s) {\n      const double w"),
+    "tree_excludes_self": ("int j = i;", "int j = parent[i];"),
+    "tree_parent_only": ("j = parent[j];", "j = (j == i) ? parent[j] : -1;"),
+}
+
+
+def _pins_pass():
+    """A compact run of the pins; False at the first disagreement."""
+    try:
+        for dtype in ("fp32", "bf16"):
+            q, k, v, vis = _rand_case(1, T=5, Hq=4, Hkv=2, D=8, n=12, dtype=dtype)
+            vis[:, 0] = True
+            out, lse = oracle.masked_attention(q, k, v, vis, 0.35)
+            tout, tlse = twin.attention(_f64(q).tolist(), _f64(k).tolist(), _f64(v).tolist(), vis.tolist(), 0.35)
+            if not (np.allclose(out, tout, atol=1e-10) and np.allclose(lse, tlse, atol=1e-10)):
+                return False
+            ref, ref_lse = _sdpa(q, k, v, vis, 0.35)
+            if not (np.allclose(out, ref, atol=1e-10) and np.allclose(lse, ref_lse, atol=1e-10)):
+                return False
+        # divide-and-aggregate exactness
+        q, k, v, vis = _rand_case(2, T=4, Hq=2, Hkv=1, D=8, n=14)
+        vis[:, :6] = True
+        full = oracle.masked_attention(q, k, v, vis, 0.5)
+        for cuts in ([0, 6, 14], [0, 3, 9, 14]):
+            part = _prefix_tree_split(q, k, v, vis, 0.5, cuts)
+            if not (np.allclose(part[0], full[0], atol=1e-10) and np.allclose(part[1], full[1], atol=1e-10)):
+                return False
+        # tree visibility against an independent ancestor walk
+        rng = np.random.default_rng(0)
+        for T in (5, 17):
+            p = W.random_parents(T, rng)
+            vis = oracle.tree_visibility(p)
+            for i in range(T):
+                if set(np.nonzero(vis[i])[0].tolist()) != twin.ancestors(p, i):
+                    return False
+        return True
+    except Exception:
+        return False
+
+
+def _build_variant(tmp_path, name, edit):
+    src = open(SRC).read()
+    if edit is not None:
+        old, new = edit
+        assert src.count(old) >= 1, f"mutant {name}: pattern not found"
+        src = src.replace(old, new, 1)
+    c = tmp_path / f"{name}.c"
+    c.write_text(src)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    return str(so)
+
+
+def test_pristine_oracle_passes_the_pins(tmp_path):
+    with oracle.swapped_library(_build_variant(tmp_path, "pristine", None)):
+        assert _pins_pass()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    with oracle.swapped_library(_build_variant(tmp_path, name, MUTANTS[name])):
+        assert not _pins_pass(), f"pins did not catch mutant {name}"
