@@ -1,0 +1,500 @@
+"""Benchmark: speculative-decoding verification attention on one GB300 per rank.
+
+One *step* is one verification pass over one batch of the workload: the draft
+tree's ancestor mask, the split-KV prefix pass, the masked draft-block pass and
+the log-sum-exp merge (the sparse workload adds the verify-index build).  The
+default workload is the 8-token draft chain over a 32768-token bf16 cache
+(B1, Hq32, Hkv8, d128).
+
+Reported (one JSON line on rank 0):
+  value        algorithmic KV bytes of all ranks / max-over-ranks time, GB/s
+               (KV bytes = (prefix keys + T) * d * 2 (K, V) * elem per kv-head)
+  tokens_per_s verified draft tokens per second
+  roofline     the verification call's achieved GB/s (CUDA events per call)
+               against the measured HBM copy bandwidth
+  e2e          the same metric through the public API with host buffers:
+               per step, H2D of the step's new inputs (q, the draft tokens'
+               K/V rows, tree parents, seqlens), the call, D2H of out + lse
+  cpu_baseline the fp64 oracle timed on this host's cores (a baseline only)
+
+Timing: W warm-up steps, then K steps replayed from CUDA graphs; each step
+reads a different copy of the inputs and the copies together exceed the L2
+cache, so no step is served from L2.  Under torchrun every rank runs its own
+replica (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------
+# device-side workload
+# ----------------------------------------------------------------------------
+
+class DeviceCase:
+    """One resident copy of a workload's inputs and outputs on the GPU."""
+
+    def __init__(self, w, va):
+        self.w = w
+        self.va = va
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+        self.q = w.q.cuda()
+        self.seqlens = i32(w.seqlens)
+        self.parent = i32(w.parent) if w.parent is not None else None
+        self.mask = (torch.from_numpy(np.ascontiguousarray(w.mask_words).view(np.int32)).cuda()
+                     if w.mask_words is not None else None)
+        if w.layout in ("dense", "sparse"):
+            self.k = w.k_cache.cuda()
+            self.v = w.v_cache.cuda()
+        else:
+            self.k = w.k_pages.cuda()
+            self.v = w.v_pages.cuda()
+            self.page_table = i32(w.page_table)
+        if w.layout == "sparse":
+            self.sd = torch.from_numpy(w.score_draft).cuda()
+            self.st = torch.from_numpy(w.score_target).cuda()
+            self.idx = torch.empty(w.B, w.Hkv, w.budget, dtype=torch.int32, device="cuda")
+            self.nidx = torch.empty(w.B, w.Hkv, dtype=torch.int32, device="cuda")
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(w.B, w.Hq, w.T, dtype=torch.float32, device="cuda")
+        shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0 if w.dtype == "bf16" else 2, w.scale)
+        self.ws = va.Workspace.for_shape(shape)
+
+    def step(self):
+        """One verification pass (all on the current stream)."""
+        va, w = self.va, self.w
+        if w.layout == "dense":
+            va.verify_attn_dense(self.q, self.k, self.v, self.seqlens, tree_parent=self.parent, tree_mask=self.mask,
+                                 out=self.out, lse=self.lse, workspace=self.ws, scale=w.scale)
+        elif w.layout == "paged":
+            va.verify_attn_paged(self.q, self.k, self.v, self.page_table, self.seqlens, tree_parent=self.parent,
+                                 tree_mask=self.mask, out=self.out, lse=self.lse, workspace=self.ws, scale=w.scale)
+        else:
+            va.verify_build_index(self.seqlens, self.sd, self.st, w.n_sink, w.window, w.m_draft, w.budget,
+                                  indices=self.idx, n_indices=self.nidx, workspace=self.ws)
+            va.verify_attn_sparse(self.q, self.k, self.v, self.seqlens, self.idx, self.nidx, tree_parent=self.parent,
+                                  tree_mask=self.mask, out=self.out, lse=self.lse, workspace=self.ws, scale=w.scale)
+
+    def resident_bytes(self):
+        tot = 0
+        for t in (self.q, self.k, self.v):
+            tot += t.numel() * t.element_size()
+        return tot
+
+
+def n_copies_for(w):
+    per_step = w.kv_bytes()
+    return int(min(8, max(2, math.ceil(3 * L2_BYTES / max(per_step, 1)))))
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        try:
+            idx = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+            phys = idx[device_index] if idx and idx[0] != "" and device_index < len(idx) else str(device_index)
+            self.path = f"/tmp/va_clocks_{os.getpid()}.csv"
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", phys, f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[0]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(num(r[1]) for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# measurement
+# ----------------------------------------------------------------------------
+
+def time_graph_steps(cases, steps, warmup, graph_steps):
+    """Capture ``graph_steps`` consecutive steps (rotating copies) in one CUDA graph;
+    replay it to run ``warmup`` + ``steps`` steps; return seconds for the timed steps."""
+    stream = torch.cuda.Stream()
+    # eager warm-up outside capture (first-call attribute setup)
+    with torch.cuda.stream(stream):
+        for i in range(max(1, len(cases))):
+            cases[i % len(cases)].step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(graph_steps):
+            cases[i % len(cases)].step()
+    reps_w = max(1, math.ceil(warmup / graph_steps))
+    reps = max(1, math.ceil(steps / graph_steps))
+    for _ in range(reps_w):
+        graph.replay()
+    torch.cuda.synchronize()
+    return graph, reps
+
+
+def per_call_durations(cases, n_calls):
+    """CUDA-event duration of each verification call, enqueued behind a spin
+    kernel so host launch latency never enters an interval."""
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
+    torch.cuda._sleep(int(50e6))  # ~25 ms of spinning while the host enqueues
+    for i in range(n_calls):
+        c = cases[i % len(cases)]
+        ev[i][0].record(stream)
+        c.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in ev]
+
+
+def e2e_measure(w, va, steps):
+    """Through the public API with host buffers: per step H2D the new inputs from
+    pinned memory, run the call, D2H out and lse, and wait for them."""
+    case = DeviceCase(w, va)
+    T, B = w.T, w.B
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    h_q = pin(w.q)
+    h_seq = pin(torch.from_numpy(np.asarray(w.seqlens, np.int32)))
+    h_par = pin(torch.from_numpy(np.asarray(w.parent, np.int32))) if w.parent is not None else None
+    h_mask = (pin(torch.from_numpy(np.ascontiguousarray(w.mask_words).view(np.int32)))
+              if w.mask_words is not None else None)
+    # the draft tokens' new K/V rows, appended at slots L_b .. L_b+T-1
+    if w.layout == "paged":
+        h_knew = [pin(torch.stack([w.k_pages[w.page_table[b, (int(w.seqlens[b]) + j) // w.page_size],
+                                             (int(w.seqlens[b]) + j) % w.page_size] for j in range(T)]))
+                  for b in range(B)]
+        h_vnew = [pin(torch.stack([w.v_pages[w.page_table[b, (int(w.seqlens[b]) + j) // w.page_size],
+                                             (int(w.seqlens[b]) + j) % w.page_size] for j in range(T)]))
+                  for b in range(B)]
+    else:
+        h_knew = [pin(w.k_cache[b, int(w.seqlens[b]): int(w.seqlens[b]) + T]) for b in range(B)]
+        h_vnew = [pin(w.v_cache[b, int(w.seqlens[b]): int(w.seqlens[b]) + T]) for b in range(B)]
+    h_out = torch.empty_like(h_q).pin_memory()
+    h_lse = torch.empty(B, w.Hq, T, dtype=torch.float32).pin_memory()
+    h2d = h_q.numel() * h_q.element_size() + h_seq.numel() * 4
+    h2d += (h_par.numel() * 4 if h_par is not None else 0) + (h_mask.numel() * 4 if h_mask is not None else 0)
+    h2d += sum(t.numel() * t.element_size() for t in h_knew + h_vnew)
+    if w.layout == "sparse":
+        h_sd = pin(torch.from_numpy(w.score_draft))
+        h_st = pin(torch.from_numpy(w.score_target))
+        h2d += 2 * h_sd.numel() * 4
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+
+    def upload():
+        case.q.copy_(h_q, non_blocking=True)
+        case.seqlens.copy_(h_seq, non_blocking=True)
+        if h_par is not None:
+            case.parent.copy_(h_par, non_blocking=True)
+        if h_mask is not None:
+            case.mask.copy_(h_mask, non_blocking=True)
+        for b in range(B):
+            L = int(w.seqlens[b])
+            if w.layout == "paged":
+                for j in range(T):
+                    pg = int(w.page_table[b, (L + j) // w.page_size])
+                    case.k[pg, (L + j) % w.page_size].copy_(h_knew[b][j], non_blocking=True)
+                    case.v[pg, (L + j) % w.page_size].copy_(h_vnew[b][j], non_blocking=True)
+            else:
+                case.k[b, L: L + T].copy_(h_knew[b], non_blocking=True)
+                case.v[b, L: L + T].copy_(h_vnew[b], non_blocking=True)
+        if w.layout == "sparse":
+            case.sd.copy_(h_sd, non_blocking=True)
+            case.st.copy_(h_st, non_blocking=True)
+
+    def one():
+        upload()
+        case.step()
+        h_out.copy_(case.out, non_blocking=True)
+        h_lse.copy_(case.lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t0) / steps
+    va.verify_attn_check_status(case.ws)
+    return dt, h2d, d2h
+
+
+def cpu_baseline(w, target_s=12.0, max_reps=50):
+    """The fp64 oracle as it stands, on this host's cores, over whole kv-head
+    groups of the same workload until about ``target_s`` seconds of work."""
+    import oracle
+
+    q = W.bf16_bits(w.q) if w.dtype == "bf16" else w.q.numpy()
+    vis = oracle.draft_visibility(w)
+    g = w.group
+    per_key = w.D * 2 * w.elem_bytes
+    done_bytes = 0
+    groups = 0
+    t0 = time.perf_counter()
+    if w.layout == "dense":
+        k = W.bf16_bits(w.k_cache) if w.dtype == "bf16" else w.k_cache.numpy()
+        v = W.bf16_bits(w.v_cache) if w.dtype == "bf16" else w.v_cache.numpy()
+        while time.perf_counter() - t0 < target_s and groups < max_reps * w.Hkv:
+            h = groups % w.Hkv
+            oracle.attention_dense(q[:, :, h * g:(h + 1) * g], k[:, :, h:h + 1], v[:, :, h:h + 1], w.seqlens, vis,
+                                   w.scale)
+            done_bytes += int((w.seqlens.astype(np.int64) + w.T).sum()) * per_key
+            groups += 1
+        sample = f"{groups} kv-head groups of the workload (each: all {w.B} sequences x {w.T} draft tokens x {g} heads)"
+    else:
+        # whole-workload passes (paged / sparse), bounded by time
+        reps = 0
+        while time.perf_counter() - t0 < target_s and reps < max_reps:
+            oracle.verify(w)
+            done_bytes += w.kv_bytes()
+            reps += 1
+        sample = f"{reps} full passes of the workload"
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+
+def load_peak_hbm():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def dist_setup(n):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    torch.cuda.set_device(0)
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    """The oracle as the reference arm: bounded samples of the workload per step."""
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return 0
+    w = W.make_workload(args.config, seed=0)
+    secs = []
+    cb = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w, target_s=max(1.0, 30.0 / max(1, args.steps + args.warmup)), max_reps=4)
+        if i >= args.warmup:
+            secs.append(r["seconds"])
+            cb = r
+    line = {"impl": "reference", "metric": "verify-attention achieved HBM GB/s and verified tokens/s",
+            "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, None),
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": cb["value"],
+                             "unit": "GB/s"},
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(w, n_copies):
+    d = {"workload": f"{w.name}: B{w.B} T{w.T} Hq{w.Hq} Hkv{w.Hkv} d{w.D} {w.dtype} {w.layout}",
+         "batch": w.B, "draft_tokens": w.T, "prefix_len": (int(w.seqlens.min()), int(w.seqlens.max())),
+         "kv_bytes_per_step": w.kv_bytes()}
+    if n_copies is not None:
+        d["l2"] = f"inputs rotated over {n_copies} resident copies ({n_copies} x {w.kv_bytes() / 1e6:.0f} MB read) > L2"
+    return d
+
+
+def measure_config(name, va, args, want_e2e, want_cpu, rank, dist):
+    w = W.make_workload(name, seed=0)
+    n_copies = n_copies_for(w)
+    cases = [DeviceCase(w, va)] + []
+    for _ in range(n_copies - 1):
+        cases.append(DeviceCase(w, va))
+    graph_steps = min(max(args.steps, 1), 64)
+    graph, reps = time_graph_steps(cases, args.steps, args.warmup, graph_steps)
+    steps_done = reps * graph_steps
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.2 if clocks else 0)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    dt = e0.elapsed_time(e1) * 1e-3 / steps_done
+    clk = clocks.stop() if clocks else None
+    for c in cases:
+        va.verify_attn_check_status(c.ws)
+    dt_max = max_over_ranks(dt, dist)
+    world = dist.get_world_size() if dist is not None else 1
+    bytes_step = w.kv_bytes()
+    gbs = bytes_step * world / dt_max / 1e9
+    durs = per_call_durations(cases, 200)
+    call_s = statistics.mean(durs)
+    res = {"w": w, "dt": dt_max, "gbs": gbs, "tok_s": w.tokens() * world / dt_max, "call_s": call_s,
+           "call_gbs": bytes_step / call_s / 1e9, "clocks": clk, "n_copies": n_copies, "steps": steps_done}
+    if want_e2e:
+        e_dt, h2d, d2h = e2e_measure(w, va, max(20, min(args.steps, 200)))
+        e_dt = max_over_ranks(e_dt, dist)
+        res["e2e"] = {"value": round(bytes_step * world / e_dt / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": round(e_dt * 1e3, 4)}
+    if want_cpu and rank == 0:
+        res["cpu"] = cpu_baseline(w)
+    del graph, cases
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
+    ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    import speculative_decoding_verification_masked_gb300 as va
+
+    va.api.lib(build_if_missing=(rank == 0))
+    barrier(dist)
+    peak, peak_kind = load_peak_hbm()
+    main_res = measure_config(args.config, va, args, want_e2e=True, want_cpu=not args.no_cpu, rank=rank, dist=dist)
+    others = {}
+    if args.all_configs:
+        for name in W.CONFIG_NAMES:
+            if name == args.config:
+                continue
+            r = measure_config(name, va, args, want_e2e=False, want_cpu=False, rank=rank, dist=dist)
+            others[name] = {"GBps": round(r["gbs"] / world, 1), "frac_of_measured_hbm": round(r["gbs"] / world / peak, 4),
+                            "us_per_step": round(r["dt"] * 1e6, 2), "tokens_per_s": round(r["tok_s"] / world, 1),
+                            "call_us": round(r["call_s"] * 1e6, 2)}
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    w = main_res["w"]
+    line = {
+        "metric": "verify-attention achieved HBM GB/s (% of GB300 peak) and verified tokens/s",
+        "value": round(main_res["gbs"], 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": main_res["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(main_res["dt"] * 1e3, 5),
+        "tokens_per_s": round(main_res["tok_s"], 1),
+        "frac_of_hbm_peak": round(main_res["gbs"] / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/k/v, seeded trees/page tables/scores)",
+        "config": config_dict(w, main_res["n_copies"]),
+        "roofline": {"bound": "hbm", "achieved": round(main_res["call_gbs"], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(main_res["call_gbs"] / peak, 4), "traffic": None,
+                     "kernel": "verify_attn call (split-KV attention kernel + PDL-chained LSE combine)",
+                     "call_us": round(main_res["call_s"] * 1e6, 3), "peak_kind": peak_kind},
+        "e2e": main_res.get("e2e"),
+        "gpu_launches": main_res["steps"] * 2,
+        "clocks": main_res["clocks"],
+    }
+    if "cpu" in main_res:
+        line["cpu_baseline"] = main_res["cpu"]
+    if others:
+        line["other_configs"] = others
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

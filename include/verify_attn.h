@@ -1,0 +1,206 @@
+/*
+ * verify_attn.h -- C ABI of libverify_attn.so: speculative-decoding
+ * verification attention on GB300 (sm_103a).
+ *
+ * T draft tokens of each sequence (a chain, a token tree given by parent
+ * pointers, or a masked draft block) attend to the sequence's committed KV
+ * cache and, under a bitmask, to one another.  The library computes it the
+ * divide-and-aggregate way of LongSpec (section 2.C, "Hybrid Tree Attention"):
+ * an unmasked split-KV pass over the cached prefix, a masked pass over the
+ * draft block, and an exact log-sum-exp merge of the partial results.  The
+ * prefix can be a contiguous cache, a paged cache behind a block table
+ * (HiSpec, section 2, batched inference with paged attention), or a
+ * fixed-size verify index set inside the full cache (Dustin, sections 1 and 3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor argument is a DEVICE pointer to memory the caller
+ *   allocated and owns; the library never allocates, frees or keeps a pointer
+ *   after the call returns.  Only `shape` and the scalar arguments live on the
+ *   host.  `workspace` is caller-owned device scratch of at least
+ *   verify_attn_workspace_size() bytes, 256-byte aligned, initialised once with
+ *   verify_attn_workspace_init() and reusable by later calls on the same stream.
+ *   Calls that run concurrently (different streams) need separate workspaces.
+ * Streams.  Every call only enqueues work on `stream` (NULL = legacy default
+ *   stream) and returns; nothing synchronises except verify_attn_check_status.
+ * Layouts (row-major, contiguous unless a stride is given):
+ *   q, out       [B][T][Hq][D]        element type shape->dtype
+ *   lse          [B][Hq][T]           fp32, natural logarithm
+ *   dense cache  [B][max_cache_len][Hkv][D]
+ *   pages        [num_pages][page_size][Hkv][D]
+ *   seqlens      [B] int32            committed prefix length L_b of sequence b
+ *   tree_parent  [B][T] int32         -1 for a root, else 0 <= parent[i] < i
+ *   tree_mask    [B][T][W] uint32     W = ceil(T/32); bit j%32 of word j/32 of
+ *                                     row i set = draft token i sees draft token j
+ *   positions    [B][T] int32         reserved (see below)
+ * Draft keys.  The T draft tokens' keys and values are already in the cache at
+ *   logical slots L_b .. L_b+T-1 (append, then verify; rejected entries are
+ *   dropped afterwards).
+ * GQA.  Query head h reads kv head h / (Hq/Hkv).
+ * Draft visibility.  Exactly one of tree_parent / tree_mask may be non-NULL.
+ *   With tree_parent, token i sees itself and its ancestors (computed inside
+ *   the attention kernel).  With tree_mask, the bits decide.  With both NULL,
+ *   the draft block is causal (a chain).  Every draft token sees the whole
+ *   prefix (the cache part carries no mask).
+ * Rows with no visible key (only possible with L_b = 0 and an empty mask row)
+ *   get out = 0 and lse = -inf.
+ * Errors.  A call returns VA_OK or an error code and never aborts.  Argument
+ *   errors are found on the host before anything is enqueued.  Values that
+ *   only the device can see (a seqlen beyond the cache, a page-table entry or
+ *   verify index out of range, a bounded wait that ran out) are recorded in a
+ *   status word inside the workspace; the kernel clamps or skips the bad value
+ *   and finishes, so the output is then undefined but no fault occurs.
+ *   verify_attn_check_status() reads and clears that word.
+ *   verify_attn_last_error() describes the last error of the calling thread.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *va_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  VA_OK = 0,
+  VA_ERR_INVALID_ARG = 1,   /* bad pointer, size or combination of arguments */
+  VA_ERR_UNSUPPORTED = 2,   /* valid but outside what this build supports */
+  VA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+  VA_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  VA_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
+  VA_ERR_DEVICE_BOUNDS = 6  /* device: seqlen / page / index out of range */
+} va_status;
+
+typedef enum { VA_DTYPE_BF16 = 0, VA_DTYPE_FP32 = 2 } va_dtype;
+
+typedef enum { VA_LAYOUT_DENSE = 0, VA_LAYOUT_PAGED = 1, VA_LAYOUT_SPARSE = 2 } va_layout;
+
+/* Problem shape.  Supported: 1 <= T <= 64; Hq % Hkv == 0; bf16 with D in
+ * {64, 128}; fp32 with D = 64; B * Hkv * ceil(Hq/Hkv*T / 64) <= 2048. */
+typedef struct {
+  int B;         /* sequences in the batch */
+  int T;         /* draft tokens per sequence */
+  int Hq;        /* query heads */
+  int Hkv;       /* key/value heads */
+  int D;         /* head dimension */
+  va_dtype dtype;/* element type of q, k, v and out */
+  float scale;   /* score scale (1/sqrt(D) for standard attention) */
+} va_shape;
+
+/* Bytes of workspace the attention calls need for `shape` on the CURRENT
+ * device (it depends on the device's SM count).  0 on invalid shape. */
+size_t verify_attn_workspace_size(const va_shape *shape);
+
+/* Clear the workspace's status word and bookkeeping (enqueued on `stream`).
+ * Call once after allocating a workspace and after an error status. */
+va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream stream);
+
+/*
+ * Verification attention over a dense contiguous cache.
+ * LongSpec section 2.C: unmasked split-KV pass over the L_b cached keys
+ * (FlashAttention-style, no mask), masked pass over the T draft keys at slots
+ * L_b..L_b+T-1, exact log-sum-exp merge.  Requires L_b + T <= max_cache_len
+ * (checked on the device).  positions may be NULL; it is reserved for a fused
+ * rotary embedding and is not read by this version (q and k must already
+ * carry their positional rotation).
+ */
+va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_cache,
+                            const void *v_cache, int max_cache_len, const int32_t *seqlens,
+                            const int32_t *tree_parent, const uint32_t *tree_mask,
+                            const int32_t *positions, void *out, float *lse, void *workspace,
+                            size_t ws_bytes, va_stream stream);
+
+/*
+ * Verification attention over a paged cache (HiSpec section 2: paged attention
+ * with block tables, so each sequence of a batch can accept a different
+ * number of tokens without padding).  Logical slot p of sequence b lives at
+ * page page_table[b][p / page_size], row p % page_size.  The draft keys are
+ * logical slots L_b..L_b+T-1.  Requires L_b + T <= max_pages_per_seq *
+ * page_size and 0 <= page < num_pages for every page read (device-checked).
+ * page_size must be a power of two between 1 and 1024.
+ */
+va_status verify_attn_paged(const va_shape *shape, const void *q, const void *k_pages,
+                            const void *v_pages, int num_pages, int page_size,
+                            const int32_t *page_table, int max_pages_per_seq,
+                            const int32_t *seqlens, const int32_t *tree_parent,
+                            const uint32_t *tree_mask, const int32_t *positions, void *out,
+                            float *lse, void *workspace, size_t ws_bytes, va_stream stream);
+
+/*
+ * Sparse verification (Dustin sections 1 and 3): the prefix part attends only
+ * to the cache rows listed in the verify set of its (sequence, kv-head); the
+ * cache itself is not compacted.  indices [B][Hkv][max_indices] int32 with
+ * n_indices [B][Hkv] valid entries each, every entry in [0, L_b) (device
+ * checked); order does not matter for the result.  The draft block is always
+ * read from the dense slots L_b..L_b+T-1 under the draft mask.
+ */
+va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k_cache,
+                             const void *v_cache, int max_cache_len, const int32_t *seqlens,
+                             const int32_t *indices, const int32_t *n_indices, int max_indices,
+                             const int32_t *tree_parent, const uint32_t *tree_mask,
+                             const int32_t *positions, void *out, float *lse, void *workspace,
+                             size_t ws_bytes, va_stream stream);
+
+/*
+ * Exact log-sum-exp merge of partial attentions of the same rows (LongSpec
+ * 2.C, the log-sum-exp fusion): lse = ln sum_s exp(lse_s), out = sum_s
+ * exp(lse_s - lse) * o_s.  o_parts [n_parts][n_rows][D] fp32 (each part
+ * normalised over its own keys), lse_parts [n_parts][n_rows] fp32 natural
+ * log (-inf = empty part) -> out [n_rows][D] of out_dtype, lse [n_rows] fp32
+ * (lse may be NULL).  Exposed for merging parts computed elsewhere, e.g. by
+ * other ranks of a context-parallel split.  D in {64, 128}, n_parts <= 1024.
+ */
+va_status verify_attn_combine(int n_rows, int n_parts, int D, const float *o_parts,
+                              const float *lse_parts, va_dtype out_dtype, void *out, float *lse,
+                              va_stream stream);
+
+/*
+ * Ancestor-or-self bitmask of token trees (LongSpec 1.3 and 2.C: every branch
+ * of the speculation tree attends to its own path).  parent [B][T] int32 as
+ * above -> mask [B][T][ceil(T/32)] uint32.  1 <= T <= 64.  A parent entry
+ * that breaks -1 <= parent[i] < i is recorded as VA_ERR_DEVICE_BOUNDS in the
+ * status word of `workspace` (which may be NULL to skip recording) and its
+ * row is cut at that node.
+ */
+va_status verify_tree_mask_from_parents(int B, int T, const int32_t *parent, uint32_t *mask,
+                                        void *workspace, va_stream stream);
+
+/*
+ * Fixed-size verify index set (Dustin section 1, hybrid attention
+ * aggregation), per (sequence b, kv-head h) with L = seqlens[b]:
+ *   I = {0..n_sink-1} U {L-window..L-1}
+ *       U top-m_draft positions of score_draft among the other positions
+ *       U the highest score_target positions among those still unchosen,
+ *         until |I| = min(budget, L),
+ * clipped to [0, L), written sorted ascending to indices[b][h][0..n) with the
+ * tail of the row set to -1, and n to n_indices[b][h].  Equal scores are
+ * taken in increasing position order; -0.0 and +0.0 count as equal; scores
+ * must not be NaN.  score_* are fp32 [B][Hkv][score_stride].  Requires
+ * budget >= n_sink + window, L <= score_stride and L <= 131072 (a longer L is
+ * recorded as VA_ERR_DEVICE_BOUNDS and clamped).  `workspace` (may be NULL)
+ * receives device-side errors.
+ */
+va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
+                             const float *score_target, int score_stride, int n_sink, int window,
+                             int m_draft, int budget, int32_t *indices, int32_t *n_indices,
+                             void *workspace, va_stream stream);
+
+/* Wait for `stream`, read and clear the device status word of `workspace`.
+ * Returns VA_OK or the first device-side error recorded since the last check. */
+va_status verify_attn_check_status(void *workspace, va_stream stream);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char *verify_attn_last_error(void);
+
+/* Library version string, e.g. "verify_attn 0.1 sm_103a". */
+const char *verify_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

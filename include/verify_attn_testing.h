@@ -1,0 +1,29 @@
+/*
+ * verify_attn_testing.h -- test hooks of libverify_attn.so (not part of the
+ * compute API).
+ */
+#ifndef VERIFY_ATTN_TESTING_H
+#define VERIFY_ATTN_TESTING_H
+
+#include "verify_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Exercise the bounded-wait error path without hanging anything: launches one
+ * kernel that waits on an mbarrier no one ever arrives on, for at most wait_ns
+ * nanoseconds (0 < wait_ns <= 1e8), after which the kernel records
+ * VA_ERR_TIMEOUT in the status word of `workspace` and exits.  A following
+ * verify_attn_check_status() on the same stream returns VA_ERR_TIMEOUT.
+ * The library has no counterpart in the method: it tests the error path that
+ * every pipeline wait of the attention kernel relies on.
+ */
+va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long wait_ns, va_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_TESTING_H */

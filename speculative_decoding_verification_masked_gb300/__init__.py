@@ -1,0 +1,19 @@
+"""GB300-native speculative-decoding verification attention.
+
+The compute lives in libverify_attn.so (hand-written sm_103a CUDA, C ABI in
+include/verify_attn.h); this package builds it in-tree and binds it.
+"""
+from .api import (  # noqa: F401
+    VerifyAttnError,
+    Workspace,
+    make_shape,
+    verify_attn_check_status,
+    verify_attn_combine,
+    verify_attn_dense,
+    verify_attn_paged,
+    verify_attn_sparse,
+    verify_build_index,
+    verify_tree_mask_from_parents,
+    version,
+    workspace_size,
+)

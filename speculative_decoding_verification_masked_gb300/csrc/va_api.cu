@@ -1,0 +1,420 @@
+// C ABI of libverify_attn: argument validation, workspace planning, launches,
+// device status and error reporting.  See include/verify_attn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "va_common.cuh"
+#include "va_kernels.h"
+#include "verify_attn_testing.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+va_status fail(va_status code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+va_status fail(va_status code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+va_status ok() {
+  g_last_error.clear();
+  return VA_OK;
+}
+
+va_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(VA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxSegments = 2048;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char *s = getenv("VA_WAIT_LIMIT_NS");
+    if (s != nullptr && *s) {
+      const unsigned long long x = strtoull(s, nullptr, 10);
+      if (x > 0) return (uint64_t)x;
+    }
+    return kDefaultWaitNs;
+  }();
+  return v;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a dense cache [rows = B * len][Hkv][D]: boxes of 64 tokens x
+// one kv-head x 128 bytes of the head dimension, 128-byte swizzled.
+bool encode_cache_map(CUtensorMap *m, const void *base, va_dtype dt, int D, int Hkv, long long rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint32_t es = dt == VA_DTYPE_BF16 ? 2 : 4;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
+  const cuuint32_t box[3] = {128 / es, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, dt == VA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count(int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static std::mutex mu;
+  static int cache[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  if (dev_out) *dev_out = dev;
+  return cache[dev];
+}
+
+// Row blocking of the packed (group * T) query rows of one kv-head.
+struct RowPlan {
+  int R, RG, NRB, rows_pad, S, use_tc;
+};
+
+constexpr bool kTcValidated = false;  // tcgen05 path not yet validated on hardware
+
+// Kernel choice and row blocking.  More than 64 packed rows (bf16, D 128) go to
+// the tcgen05 kernel in blocks of up to 256 rows (two 128-row M-tiles); the
+// rest to the mma.sync kernel in blocks of 16, 32 or 64 rows.
+RowPlan row_plan(const va_shape &s) {
+  RowPlan r;
+  r.R = (s.Hq / s.Hkv) * s.T;
+  r.use_tc = 0;
+  if (s.dtype == VA_DTYPE_FP32) {
+    r.RG = 4;
+    r.rows_pad = 64;
+  } else if (kTcValidated && s.D == 128 && r.R > 64) {
+    r.use_tc = 1;
+    r.RG = 4;
+    r.rows_pad = r.R > 128 ? 256 : 128;
+  } else {
+    r.RG = r.R <= 16 ? 1 : (r.R <= 32 ? 2 : 4);
+    r.rows_pad = 16 * r.RG;
+  }
+  r.NRB = (r.R + r.rows_pad - 1) / r.rows_pad;
+  r.S = s.B * s.Hkv * r.NRB;
+  return r;
+}
+
+va_status check_shape(const va_shape *s) {
+  if (s == nullptr) return fail(VA_ERR_INVALID_ARG, "shape is NULL");
+  if (s->B < 1 || s->T < 1 || s->Hq < 1 || s->Hkv < 1 || s->D < 1)
+    return fail(VA_ERR_INVALID_ARG, "shape has a non-positive size (B=%d T=%d Hq=%d Hkv=%d D=%d)", s->B, s->T,
+                s->Hq, s->Hkv, s->D);
+  if (s->Hq % s->Hkv != 0) return fail(VA_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", s->Hq, s->Hkv);
+  if (s->dtype != VA_DTYPE_BF16 && s->dtype != VA_DTYPE_FP32)
+    return fail(VA_ERR_INVALID_ARG, "unknown dtype %d", (int)s->dtype);
+  if (!(s->scale > 0.f) || !isfinite(s->scale)) return fail(VA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (s->T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d draft tokens; at most 64 are supported", s->T);
+  if (s->dtype == VA_DTYPE_BF16 && s->D != 64 && s->D != 128)
+    return fail(VA_ERR_UNSUPPORTED, "bf16 supports D in {64, 128}, got %d", s->D);
+  if (s->dtype == VA_DTYPE_FP32 && s->D != 64) return fail(VA_ERR_UNSUPPORTED, "fp32 supports D = 64, got %d", s->D);
+  const RowPlan rp = row_plan(*s);
+  if ((long long)s->B * s->Hkv * rp.NRB > kMaxSegments)
+    return fail(VA_ERR_UNSUPPORTED, "B*Hkv*row_blocks = %lld exceeds %d", (long long)s->B * s->Hkv * rp.NRB,
+                kMaxSegments);
+  return VA_OK;
+}
+
+size_t workspace_bytes(const va_shape &s, int sm_count) {
+  const RowPlan rp = row_plan(s);
+  const int slots = rp.S + sm_count;
+  return va::ws_layout(rp.S, slots, rp.rows_pad, s.D).total;
+}
+
+struct Common {
+  const va_shape *shape;
+  const void *q;
+  const int32_t *seqlens, *parent;
+  const uint32_t *mask;
+  void *out;
+  float *lse;
+  void *ws;
+  size_t ws_bytes;
+};
+
+va_status check_common(const Common &c) {
+  va_status st = check_shape(c.shape);
+  if (st != VA_OK) return st;
+  if (c.q == nullptr || c.seqlens == nullptr || c.out == nullptr || c.lse == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "q, seqlens, out and lse must not be NULL");
+  if (c.parent != nullptr && c.mask != nullptr)
+    return fail(VA_ERR_INVALID_ARG, "give tree_parent or tree_mask, not both");
+  const size_t el = c.shape->dtype == VA_DTYPE_BF16 ? 2 : 4;
+  const size_t out_align = el == 2 ? 8 : 4;
+  if (!aligned(c.q, 16) || !aligned(c.out, out_align))
+    return fail(VA_ERR_INVALID_ARG, "q must be 16-byte aligned and out %zu-byte aligned", out_align);
+  if (c.ws == nullptr) return fail(VA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(c.ws, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  return VA_OK;
+}
+
+va_status run_attention(const Common &c, int layout, const void *k, const void *v, int len_cap, int num_pages,
+                        int page_size, const int32_t *page_table, int max_pages, const int32_t *indices,
+                        const int32_t *n_indices, int max_indices, cudaStream_t stream) {
+  const va_shape &s = *c.shape;
+  int dev = 0;
+  const int sms = device_sm_count(&dev);
+  if (sms <= 0) return fail(VA_ERR_CUDA, "no usable CUDA device");
+  const size_t need = workspace_bytes(s, sms);
+  if (c.ws_bytes < need)
+    return fail(VA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", c.ws_bytes, need);
+  const RowPlan rp = row_plan(s);
+
+  va::AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.B = s.B;
+  p.T = s.T;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.D = s.D;
+  p.R = rp.R;
+  p.RG = rp.RG;
+  p.NRB = rp.NRB;
+  p.S = rp.S;
+  p.rows_pad = rp.rows_pad;
+  p.use_tc = rp.use_tc;
+  p.scale = s.scale;
+  p.dtype = s.dtype;
+  p.layout = layout;
+  p.q = c.q;
+  p.k = k;
+  p.v = v;
+  p.len_cap = len_cap;
+  p.num_pages = num_pages;
+  p.page_shift = 0;
+  while ((1 << p.page_shift) < page_size) ++p.page_shift;
+  p.max_pages = max_pages;
+  p.page_table = page_table;
+  p.seqlens = c.seqlens;
+  p.indices = indices;
+  p.n_indices = n_indices;
+  p.max_indices = max_indices;
+  p.parent = c.parent;
+  p.mask = c.mask;
+  p.mask_words = (s.T + 31) / 32;
+  p.out = c.out;
+  p.lse = c.lse;
+  const va::WsLayout wl = va::ws_layout(rp.S, rp.S + sms, rp.rows_pad, s.D);
+  uint8_t *ws = static_cast<uint8_t *>(c.ws);
+  p.status = reinterpret_cast<int *>(ws);
+  p.meta = reinterpret_cast<int2 *>(ws + wl.meta_off);
+  p.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
+  p.o_part = reinterpret_cast<float *>(ws + wl.o_off);
+  p.wait_ns = wait_limit_ns();
+
+  // key tiles an upper bound can produce; the grid never exceeds them
+  long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
+  const long long tiles_cap = (long long)rp.S * ((keys_cap + 63) / 64);
+  if (tiles_cap >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "problem too large (%lld key tiles)", tiles_cap);
+  const int grid = (int)(tiles_cap < sms ? tiles_cap : sms);
+  if (va::attn_smem_required(p) > 232448) return fail(VA_ERR_UNSUPPORTED, "shared memory plan too large");
+  CUtensorMap tmk, tmv;
+  memset(&tmk, 0, sizeof tmk);
+  memset(&tmv, 0, sizeof tmv);
+  if (layout == VA_LAYOUT_DENSE) {
+    const long long rows = (long long)s.B * len_cap;
+    if (rows >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "B * max_cache_len must be below 2^31");
+    if (!encode_cache_map(&tmk, k, s.dtype, s.D, s.Hkv, rows) || !encode_cache_map(&tmv, v, s.dtype, s.D, s.Hkv, rows))
+      return fail(VA_ERR_CUDA, "could not encode the TMA tensor maps of the cache");
+  }
+  cudaError_t e = va::launch_attention(p, tmk, tmv, grid < 1 ? 1 : grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t verify_attn_workspace_size(const va_shape *shape) {
+  if (check_shape(shape) != VA_OK) return 0;
+  const int sms = device_sm_count(nullptr);
+  if (sms <= 0) return 0;
+  return workspace_bytes(*shape, sms);
+}
+
+va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream stream) {
+  if (workspace == nullptr || ws_bytes < va::kHeaderBytes) return fail(VA_ERR_WORKSPACE, "workspace too small");
+  if (!aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, va::kHeaderBytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace init");
+  return ok();
+}
+
+va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_cache, const void *v_cache,
+                            int max_cache_len, const int32_t *seqlens, const int32_t *tree_parent,
+                            const uint32_t *tree_mask, const int32_t *positions, void *out, float *lse,
+                            void *workspace, size_t ws_bytes, va_stream stream) {
+  (void)positions;
+  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  va_status st = check_common(c);
+  if (st != VA_OK) return st;
+  if (k_cache == nullptr || v_cache == nullptr) return fail(VA_ERR_INVALID_ARG, "k_cache and v_cache must not be NULL");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(VA_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  if (max_cache_len < shape->T)
+    return fail(VA_ERR_INVALID_ARG, "max_cache_len=%d is smaller than T=%d", max_cache_len, shape->T);
+  return run_attention(c, VA_LAYOUT_DENSE, k_cache, v_cache, max_cache_len, 0, 1, nullptr, 0, nullptr, nullptr, 0,
+                       (cudaStream_t)stream);
+}
+
+va_status verify_attn_paged(const va_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                            int num_pages, int page_size, const int32_t *page_table, int max_pages_per_seq,
+                            const int32_t *seqlens, const int32_t *tree_parent, const uint32_t *tree_mask,
+                            const int32_t *positions, void *out, float *lse, void *workspace, size_t ws_bytes,
+                            va_stream stream) {
+  (void)positions;
+  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  va_status st = check_common(c);
+  if (st != VA_OK) return st;
+  if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "k_pages, v_pages and page_table must not be NULL");
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16)) return fail(VA_ERR_INVALID_ARG, "pages must be 16-byte aligned");
+  if (page_size < 1 || page_size > 1024 || (page_size & (page_size - 1)) != 0)
+    return fail(VA_ERR_INVALID_ARG, "page_size=%d must be a power of two in [1, 1024]", page_size);
+  if (num_pages < 1 || max_pages_per_seq < 1) return fail(VA_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
+  const long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap < shape->T) return fail(VA_ERR_INVALID_ARG, "max_pages_per_seq*page_size is smaller than T");
+  if (cap >= (1ll << 30)) return fail(VA_ERR_UNSUPPORTED, "max_pages_per_seq*page_size too large");
+  return run_attention(c, VA_LAYOUT_PAGED, k_pages, v_pages, (int)cap, num_pages, page_size, page_table,
+                       max_pages_per_seq, nullptr, nullptr, 0, (cudaStream_t)stream);
+}
+
+va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k_cache, const void *v_cache,
+                             int max_cache_len, const int32_t *seqlens, const int32_t *indices,
+                             const int32_t *n_indices, int max_indices, const int32_t *tree_parent,
+                             const uint32_t *tree_mask, const int32_t *positions, void *out, float *lse,
+                             void *workspace, size_t ws_bytes, va_stream stream) {
+  (void)positions;
+  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  va_status st = check_common(c);
+  if (st != VA_OK) return st;
+  if (k_cache == nullptr || v_cache == nullptr || indices == nullptr || n_indices == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "k_cache, v_cache, indices and n_indices must not be NULL");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return fail(VA_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  if (max_cache_len < shape->T)
+    return fail(VA_ERR_INVALID_ARG, "max_cache_len=%d is smaller than T=%d", max_cache_len, shape->T);
+  if (max_indices < 0) return fail(VA_ERR_INVALID_ARG, "max_indices must be >= 0");
+  return run_attention(c, VA_LAYOUT_SPARSE, k_cache, v_cache, max_cache_len, 0, 1, nullptr, 0, indices, n_indices,
+                       max_indices, (cudaStream_t)stream);
+}
+
+va_status verify_attn_combine(int n_rows, int n_parts, int D, const float *o_parts, const float *lse_parts,
+                              va_dtype out_dtype, void *out, float *lse, va_stream stream) {
+  if (n_rows < 0 || n_parts < 1) return fail(VA_ERR_INVALID_ARG, "n_rows must be >= 0 and n_parts >= 1");
+  if (D != 64 && D != 128) return fail(VA_ERR_UNSUPPORTED, "D must be 64 or 128, got %d", D);
+  if (n_parts > 1024) return fail(VA_ERR_UNSUPPORTED, "at most 1024 parts per merge, got %d", n_parts);
+  if (out_dtype != VA_DTYPE_BF16 && out_dtype != VA_DTYPE_FP32) return fail(VA_ERR_INVALID_ARG, "unknown out dtype");
+  if (o_parts == nullptr || lse_parts == nullptr || out == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "o_parts, lse_parts and out must not be NULL");
+  if (n_rows == 0) return ok();
+  cudaError_t e =
+      va::launch_combine_generic(n_rows, n_parts, D, o_parts, lse_parts, out_dtype, out, lse, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return ok();
+}
+
+va_status verify_tree_mask_from_parents(int B, int T, const int32_t *parent, uint32_t *mask, void *workspace,
+                                        va_stream stream) {
+  if (B < 1 || T < 1) return fail(VA_ERR_INVALID_ARG, "B and T must be >= 1");
+  if (T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d; at most 64 draft tokens are supported", T);
+  if (parent == nullptr || mask == nullptr) return fail(VA_ERR_INVALID_ARG, "parent and mask must not be NULL");
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = va::launch_tree_mask(B, T, parent, mask, static_cast<int *>(workspace), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tree mask launch");
+  return ok();
+}
+
+va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
+                             const float *score_target, int score_stride, int n_sink, int window, int m_draft,
+                             int budget, int32_t *indices, int32_t *n_indices, void *workspace, va_stream stream) {
+  if (B < 1 || Hkv < 1) return fail(VA_ERR_INVALID_ARG, "B and Hkv must be >= 1");
+  if (seqlens == nullptr || score_draft == nullptr || score_target == nullptr || indices == nullptr ||
+      n_indices == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "seqlens, scores, indices and n_indices must not be NULL");
+  if (n_sink < 0 || window < 0 || m_draft < 0 || budget < 1 || score_stride < 1)
+    return fail(VA_ERR_INVALID_ARG, "negative selection size or empty budget/stride");
+  if (budget < n_sink + window)
+    return fail(VA_ERR_INVALID_ARG, "budget=%d is smaller than n_sink + window = %d", budget, n_sink + window);
+  if ((long long)B * Hkv > (1ll << 30)) return fail(VA_ERR_UNSUPPORTED, "too many (sequence, head) rows");
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = va::launch_build_index(B, Hkv, seqlens, score_draft, score_target, score_stride, n_sink, window,
+                                         m_draft, budget, indices, n_indices, static_cast<int *>(workspace),
+                                         (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "index launch");
+  return ok();
+}
+
+va_status verify_attn_check_status(void *workspace, va_stream stream) {
+  if (workspace == nullptr) return fail(VA_ERR_WORKSPACE, "workspace is NULL");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int status = 0;
+  e = cudaMemcpy(&status, workspace, sizeof status, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (status != 0) {
+    e = cudaMemset(workspace, 0, sizeof status);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    switch (status) {
+      case VA_ERR_TIMEOUT:
+        return fail(VA_ERR_TIMEOUT, "a bounded device wait ran out");
+      case VA_ERR_DEVICE_BOUNDS:
+        return fail(VA_ERR_DEVICE_BOUNDS, "device saw an out-of-range seqlen, page, index or parent");
+      default:
+        return fail((va_status)status, "device status %d", status);
+    }
+  }
+  return ok();
+}
+
+const char *verify_attn_last_error(void) { return g_last_error.c_str(); }
+
+const char *verify_attn_version(void) { return "verify_attn 0.1 sm_103a"; }
+
+// Test hook declared in verify_attn_testing.h.
+va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long wait_ns, va_stream stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "bad workspace");
+  if (wait_ns == 0 || wait_ns > 100000000ull) return fail(VA_ERR_INVALID_ARG, "wait_ns must be in (0, 0.1 s]");
+  cudaError_t e = va::launch_wait_selftest(static_cast<int *>(workspace), wait_ns, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,502 @@
+// Verification attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// for the case where the packed query rows of one kv-head (GQA group x T draft
+// tokens) exceed 64 -- e.g. a 64-node token tree with group 4 gives 256 rows.
+// Same method and work plan as verify_attn_kernel (LongSpec 2.C: unmasked
+// prefix, masked draft block, exact log-sum-exp merge; stream-K over
+// 64-key tiles), but every K/V tile read from HBM now feeds up to 256 query
+// rows through UMMA instead of warp-level mma.sync.
+//
+// Roles (10 warps when the segment has two 128-row M-tiles):
+//   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
+//                    = one TMEM lane.  Reads S from TMEM, applies the draft
+//                    bitmask, runs the online softmax, writes P (bf16) back
+//                    over S, rescales O in TMEM when the row max grows by
+//                    more than 2^8, and writes the output row.
+//   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
+//                    sparse) into a 4-stage ring (shared with the other kernel)
+//   warp 4*NMT+1     MMA issuer: S_i = Q_i K^T (M128 N64 K128, both operands in
+//                    shared memory, K-major 128B swizzle) into a double-buffered
+//                    TMEM slot, and O_i += P_i V (A = P from TMEM, B = V as an
+//                    MN-major operand); owns the TMEM allocation.
+// TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
+// Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
+// barrier sequence of all roles intact, drains and frees TMEM.
+#include <cuda.h>
+#include <math.h>
+
+#include "va_common.cuh"
+#include "va_kernels.h"
+#include "va_pipeline.cuh"
+
+namespace va {
+
+constexpr int kTcStages = 4;
+
+// ---------------------------------------------------------------------------
+// tcgen05 wrappers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor (sm_100 layout): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulate, bf16 A and B, K-major A,
+// B K-major (0) or MN-major (1), N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+      "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%"
+      "18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// shared memory plan
+// ---------------------------------------------------------------------------
+template <int NMT>
+struct TcSmem {
+  static constexpr int kQBytes = NMT * 2 * 128 * 128;  // NMT M-tiles x 2 columns x 128 rows x 128 B
+  static constexpr int kStageBytes = StageGeom<__nv_bfloat16, 128>::kStageBytes;
+  static constexpr int kStagesOff = kQBytes;
+  static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
+  // barriers: full[4], empty[4], s_full[2][2], p_full[2][2], o_done[2], drain
+  static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kTstartOff = kMiscOff + 16;
+  static constexpr int kThreads = (4 * NMT + 2) * 32;
+};
+
+// Offset of chunk c (16 B) of row r in a 128-row, 128B-swizzled Q tile pair.
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int NMT>
+__global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
+    verify_attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
+  using SM = TcSmem<NMT>;
+  using Geo = StageGeom<__nv_bfloat16, 128>;
+  constexpr int D = 128;
+  constexpr int NS = kTcStages;
+  constexpr int kSoftThreads = 128 * NMT;
+  constexpr int kProducerWarp = 4 * NMT;
+  constexpr int kMmaWarp = 4 * NMT + 1;
+  constexpr int kBarQ = 1, kBarSoft = 2, kBarEnd = 3;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t *sQ = smem;
+  uint8_t *stages = smem + SM::kStagesOff;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBarOff);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + NS;
+  uint64_t *s_full = bars + 2 * NS;      // [i][b] at 2*i + b
+  uint64_t *p_full = bars + 2 * NS + 4;  // [i][b]
+  uint64_t *o_done = bars + 2 * NS + 8;  // [i]
+  uint64_t *drain = bars + 2 * NS + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
+  int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  const bool use_tma = p.layout == VA_LAYOUT_DENSE;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = blockIdx.x;
+
+  pdl_launch_dependents();
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, use_tma ? 1 : 32);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 128);
+    }
+    mbar_init(o_done + 0, 1);
+    mbar_init(o_done + 1, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const CtaRange cr = plan_cta(p, tstart);  // contains __syncthreads
+  if (c >= cr.G) return;
+  const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
+
+  if (warp == kProducerWarp) {
+    bool pok = true;
+    produce_tiles<__nv_bfloat16, D, NS>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag, use_tma, pok);
+    return;
+  }
+
+  // TMEM: 512 columns, allocated by the MMA warp
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  named_bar_sync(kBarEnd, kSoftThreads + 32);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const float cl2 = p.scale * kLog2e;
+  const int group = p.Hq / p.Hkv;
+
+  if (warp == kMmaWarp) {
+    // ================================ MMA issuer ================================
+    const uint32_t id_s = umma_idesc(128, 64, 0);
+    const uint32_t id_o = umma_idesc(128, 128, 1);
+    int it = 0, jt = 0;
+    bool ok = true;
+    auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
+      if (ok && *abort_flag) ok = false;
+      if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
+        record_status(p.status, VA_ERR_TIMEOUT);
+        *abort_flag = 1;
+        ok = false;
+      }
+    };
+    // make stage `st` of tile lt ready for the MMAs: wait for it; on the dense
+    // path zero the V rows past the segment end (TMA brought whole boxes)
+    auto acquire_stage = [&](int st, uint32_t ph, int lt, const Seg &g) {
+      wait_ok(full + st, ph);
+      if (ok && use_tma && lt * kTK + kTK > g.nkeys) {
+        uint8_t *vt = stages + st * Geo::kStageBytes + Geo::kTileBytes;
+        for (int e = lane; e < kTK * Geo::kChunks; e += 32) {
+          const int r = e / Geo::kChunks;
+          if (lt * kTK + r >= g.nkeys) *reinterpret_cast<uint4 *>(vt + swz(r, e % Geo::kChunks)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+    };
+    auto issue_s = [&](int i, int b, int st) {  // S_i(b) = Q_i K^T
+      if (!ok || lane != 0) return;
+      tc_fence_after();
+      const uint32_t q0 = smem_u32(sQ) + i * 32768;
+      const uint32_t k0 = smem_u32(stages + st * Geo::kStageBytes);
+      const uint32_t dS = tmem + 256 + 64 * (2 * i + b);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t a = umma_sdesc(q0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+        const uint64_t bb = umma_sdesc(k0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+        umma_ss(dS, a, bb, id_s, ks > 0);
+      }
+      umma_commit(s_full + 2 * i + b);
+    };
+    auto issue_pv = [&](int i, int b, int st, bool first, bool exact) {  // O_i += P_i V
+      if (!ok || lane != 0) return;
+      tc_fence_after();
+      const uint32_t v0 = smem_u32(stages + st * Geo::kStageBytes + Geo::kTileBytes);
+      const uint32_t aP = tmem + 256 + 64 * (2 * i + b);
+      const uint32_t dO = tmem + 128 * i;
+#pragma unroll
+      for (int kk = 0; kk < kTK / 16; ++kk) {
+        const uint64_t bb = umma_sdesc(v0 + kk * 2048, 8192, 1024);
+        umma_ts(dO, aP + kk * 8, bb, id_o, (!first || kk > 0) ? 1u : 0u);
+        if (exact) umma_ts(dO, aP + 32 + kk * 8, bb, id_o, 1u);
+      }
+      umma_commit(o_done + i);
+    };
+
+    for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
+      const Seg g = seg_info(p, s, false);
+      const int lt0 = max(tstart[s], t0) - tstart[s];
+      const int lt1 = min(tstart[s + 1], t1) - tstart[s];
+      named_bar_sync(kBarQ, kSoftThreads + 32);  // Q of this segment is in shared memory
+      // prologue: S of the first tile
+      acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
+      for (int i = 0; i < NMT; ++i) issue_s(i, jt & 1, it % NS);
+      for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
+        const int st = it % NS;
+        const int b = jt & 1;
+        const uint32_t pph = (uint32_t)(jt >> 1) & 1u;
+        const bool has_next = lt + 1 < lt1;
+        const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
+        const int st_n = (it + 1) % NS;
+        for (int i = 0; i < NMT; ++i) {
+          wait_ok(p_full + 2 * i + b, pph);
+          issue_pv(i, b, st, lt == lt0, exact);
+          if (i == NMT - 1 && ok && lane == 0) umma_commit(empty + st);  // K/V of this tile no longer needed
+          if (has_next) {
+            if (i == 0) acquire_stage(st_n, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
+            issue_s(i, b ^ 1, st_n);
+          }
+        }
+      }
+    }
+    // drain: every MMA this warp issued has finished before TMEM is released
+    if (lane == 0) umma_commit(drain);
+    mbar_wait(drain, 0u, p.wait_ns);
+    tc_fence_before();
+    named_bar_sync(kBarEnd, kSoftThreads + 32);
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    return;
+  }
+
+  // ============================ softmax warpgroups ============================
+  const int mi = warp >> 2;                 // M-tile of this warpgroup
+  const int r = (warp & 3) * 32 + lane;     // row in the M-tile = TMEM lane
+  const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t tO = tmem + lane_bits + 128 * mi;
+  bool ok = true;
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
+    if (ok && *abort_flag) ok = false;
+    if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
+      record_status(p.status, VA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      ok = false;
+    }
+  };
+  int jt = 0;
+  for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
+    const Seg g = seg_info(p, s, false);
+    const int lt0 = max(tstart[s], t0) - tstart[s];
+    const int lt1 = min(tstart[s + 1], t1) - tstart[s];
+    const int first_cta = owner_cta(tstart[s], cr.total, cr.G);
+    const int n_parts = owner_cta(tstart[s + 1] - 1, cr.total, cr.G) - first_cta + 1;
+    if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
+
+    // ---- Q of this segment into shared memory (both warpgroups) ----
+    named_bar_sync(kBarSoft, kSoftThreads);  // previous segment's MMAs have all completed
+    {
+      const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+      for (int e = tid; e < NMT * 128 * 16; e += kSoftThreads) {
+        const int m = e / (128 * 16);
+        const int row = (e / 16) % 128;
+        const int ch = e % 16;
+        const int rr = g.rb * p.rows_pad + m * 128 + row;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (rr < p.R) {
+          const int t = rr / group;
+          const int hq = g.hkv * group + rr % group;
+          v = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + ch);
+        }
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch)) = v;
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_arrive(kBarQ, kSoftThreads + 32);
+
+    const int rr = g.rb * p.rows_pad + mi * 128 + r;
+    const bool rvalid = rr < p.R;
+    const int t = rvalid ? rr / group : 0;
+    const int hq = g.hkv * group + (rvalid ? rr % group : 0);
+    uint64_t rmask = 0;
+    if (lt1 * kTK > g.n_prefix) {
+      uint64_t tl = 0, th = 0;
+      if (p.parent != nullptr) warp_tree_rows(p, g.b, tl, th);
+      rmask = draft_row(p, g.b, t, tl, th);
+    }
+    float m_used = -INFINITY;  // reference max of the exponentials (raw score units)
+    float l = 0.f;
+
+    for (int lt = lt0; lt < lt1; ++lt, ++jt) {
+      const int b = jt & 1;
+      const uint32_t tS = tmem + lane_bits + 256 + 64 * (2 * mi + b);
+      wait_ok(s_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+      tc_fence_after();
+      float sv[64];
+      {
+        uint32_t u[32];
+        tmem_ld32(tS, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(u[j]);
+        tmem_ld32(tS + 32, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(u[j]);
+      }
+      const int k0 = lt * kTK;
+      const bool masked = k0 + kTK > g.n_prefix;
+      if (masked) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int key = k0 + j;
+          bool vis = key < g.nkeys;
+          if (vis && key >= g.n_prefix) vis = (rmask >> (key - g.n_prefix)) & 1ull;
+          if (!vis) sv[j] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
+      const float m_new = fmaxf(m_used, mx);
+      if (lt == lt0) {
+        m_used = m_new;
+      } else {
+        // move the reference max only when it grew by more than 2^8 (exact either way)
+        const bool need = (m_new - m_used) * cl2 > 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          wait_ok(o_done + mi, (uint32_t)(jt - 1) & 1u);  // O holds every PV up to the previous tile
+          tc_fence_after();
+          const float alpha = need ? exp2f((m_used - m_new) * cl2) : 1.f;
+#pragma unroll
+          for (int cch = 0; cch < 4; ++cch) {
+            uint32_t u[32];
+            tmem_ld32(tO + 32 * cch, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+            tmem_st32(tO + 32 * cch, u);
+          }
+          tmem_st_wait();
+          if (need) {
+            l *= alpha;
+            m_used = m_new;
+          }
+        }
+      }
+      const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
+      uint32_t ph[32], pl[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = exp2f(fmaf(sv[2 * j], cl2, -mu));
+        const float bq = exp2f(fmaf(sv[2 * j + 1], cl2, -mu));
+        ls += a + bq;
+        split_bf16x2(a, bq, ph[j], pl[j]);
+      }
+      l += ls;
+      tmem_st32(tS, ph);
+      if (masked) tmem_st32(tS + 32, pl);  // lo parts feed a second MMA on draft tiles
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full + 2 * mi + b);
+    }
+
+    // ---- epilogue: O / l for this segment part ----
+    wait_ok(o_done + mi, (uint32_t)(jt - 1) & 1u);
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse_nat = l > 0.f ? (m_used * cl2 + log2f(l)) * kLn2 : -INFINITY;
+    const bool write = rvalid && ok;
+#pragma unroll
+    for (int cch = 0; cch < 4; ++cch) {
+      uint32_t u[32];
+      tmem_ld32(tO + 32 * cch, u);
+      tmem_ld_wait();
+      if (!write) continue;
+      if (n_parts == 1) {
+        uint4 *ob = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                              (((size_t)g.b * p.T + t) * p.Hq + hq) * D + 32 * cch);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(u[8 * q4 + 0]) * inv, __uint_as_float(u[8 * q4 + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(u[8 * q4 + 2]) * inv, __uint_as_float(u[8 * q4 + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(u[8 * q4 + 4]) * inv, __uint_as_float(u[8 * q4 + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(u[8 * q4 + 6]) * inv, __uint_as_float(u[8 * q4 + 7]) * inv);
+          ob[q4] = v;
+        }
+      } else {
+        float4 *op = reinterpret_cast<float4 *>(p.o_part +
+                                                ((size_t)(s + c) * p.rows_pad + mi * 128 + r) * D + 32 * cch);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          op[q4] = make_float4(__uint_as_float(u[4 * q4]) * inv, __uint_as_float(u[4 * q4 + 1]) * inv,
+                               __uint_as_float(u[4 * q4 + 2]) * inv, __uint_as_float(u[4 * q4 + 3]) * inv);
+      }
+    }
+    if (write) {
+      if (n_parts == 1)
+        p.lse[((size_t)g.b * p.Hq + hq) * p.T + t] = lse_nat;
+      else
+        p.lse_part[(size_t)(s + c) * p.rows_pad + mi * 128 + r] = lse_nat;
+    }
+  }
+  tc_fence_before();
+  named_bar_sync(kBarEnd, kSoftThreads + 32);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int NMT>
+static size_t tc_smem_bytes(int S) {
+  return 1024 + (size_t)TcSmem<NMT>::kTstartOff + (size_t)(S + 1) * 4;
+}
+
+size_t attn_tc_smem_required(const AttnParams &p) {
+  return p.rows_pad > 128 ? tc_smem_bytes<2>(p.S) : tc_smem_bytes<1>(p.S);
+}
+
+template <int NMT>
+static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                               cudaStream_t stream) {
+  const size_t smem = tc_smem_bytes<NMT>(p.S);
+  auto kern = verify_attn_tc_kernel<NMT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, TcSmem<NMT>::kThreads, smem, stream>>>(p, tmk, tmv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                cudaStream_t stream) {
+  return p.rows_pad > 128 ? launch_tc_t<2>(p, tmk, tmv, grid, stream) : launch_tc_t<1>(p, tmk, tmv, grid, stream);
+}
+
+}  // namespace va

@@ -1,0 +1,301 @@
+// Auxiliary kernels of the verification path:
+//  * tree_mask_kernel   -- ancestor-or-self bitmask of token trees
+//                          (LongSpec 1.3 / 2.C: each branch attends to its path)
+//  * build_index_kernel -- fixed-size verify index set (Dustin section 1)
+//  * wait_selftest_kernel -- exercises the bounded-wait error path
+#include "va_common.cuh"
+#include "va_kernels.h"
+
+namespace va {
+
+// ---------------------------------------------------------------------------
+// tree -> bitmask
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(64) tree_mask_kernel(int T, const int32_t *parent, uint32_t *mask, int *status) {
+  __shared__ int par[64];
+  const int b = blockIdx.x;
+  const int t = threadIdx.x;
+  if (t < T) {
+    int pp = __ldg(parent + (size_t)b * T + t);
+    if (pp < -1 || pp >= t) {  // the path is cut at a node whose parent is not earlier
+      record_status(status, VA_ERR_DEVICE_BOUNDS);
+      pp = -1;
+    }
+    par[t] = pp;
+  }
+  __syncthreads();
+  if (t >= T) return;
+  uint64_t row = 0;
+  for (int j = t; j >= 0; j = par[j]) row |= 1ull << j;  // par[j] < j: ends within T steps
+  const int W = (T + 31) / 32;
+  uint32_t *dst = mask + ((size_t)b * T + t) * W;
+  dst[0] = (uint32_t)row;
+  if (W > 1) dst[1] = (uint32_t)(row >> 32);
+}
+
+cudaError_t launch_tree_mask(int B, int T, const int32_t *parent, uint32_t *mask, int *status, cudaStream_t stream) {
+  tree_mask_kernel<<<B, 64, 0, stream>>>(T, parent, mask, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// verify index set (Dustin section 1): sinks + recent window + top-m of the
+// draft signal + top of the target signal, sorted ascending.
+//
+// One CTA per (sequence, kv-head).  The chosen set lives in a bitmap over
+// positions, so the output comes out sorted by a prefix count over bitmap
+// words.  Each top-k is an exact radix select on order-preserving 32-bit keys
+// (four 8-bit digits, most significant first); keys equal to the threshold are
+// taken in increasing position order, which is the tie rule.
+// ---------------------------------------------------------------------------
+constexpr int kIdxThreads = 1024;
+constexpr int kIdxMaxL = 131072;
+constexpr int kIdxBitmapWords = kIdxMaxL / 32 + 4;
+constexpr int kIdxCacheKeys = 45056;  // keys held in shared memory when L fits
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0.0 ranks with +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct IdxSmem {
+  uint32_t *bitmap;
+  uint32_t *hist;
+  int *scratch;
+  uint32_t *keys;
+};
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the
+// thread's exclusive prefix and the block total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int wv = scratch[lane];
+    int wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    scratch[32 + lane] = wi - wv;  // exclusive warp offsets
+    if (lane == 31) scratch[31] = wi;  // total (slot 31 is no longer needed)
+  }
+  __syncthreads();
+  const int res = scratch[32 + warp] + incl - v;
+  total = scratch[31];
+  __syncthreads();
+  return res;
+}
+
+// Select the k largest keys among positions [0, L) not yet in the bitmap and
+// add them to it.  k must not exceed the number of such positions.
+__device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
+  if (k <= 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool cached = L <= kIdxCacheKeys;
+  auto excluded = [&](int i) -> bool { return (sm.bitmap[i >> 5] >> (i & 31)) & 1u; };
+  if (cached) {
+    for (int i = tid; i < L; i += kIdxThreads) sm.keys[i] = excluded(i) ? 0u : order_key(__ldg(src + i));
+    __syncthreads();
+  }
+  auto key_at = [&](int i) -> uint32_t {
+    if (cached) return sm.keys[i];
+    return excluded(i) ? 0u : order_key(__ldg(src + i));
+  };
+
+  uint32_t prefix = 0, pmask = 0;
+  int kk = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) sm.hist[tid] = 0;
+    __syncthreads();
+    for (int base = 0; base < L; base += kIdxThreads) {
+      const int i = base + tid;
+      uint32_t key = 0;
+      bool valid = false;
+      if (i < L) {
+        key = key_at(i);
+        valid = key != 0u && (key & pmask) == prefix;
+      }
+      const uint32_t digit = valid ? (key >> shift) & 255u : 256u + lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (valid && lane == __ffs(peers) - 1) atomicAdd(sm.hist + digit, (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l, scanned from the top
+      int c[8];
+      int sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = (int)sm.hist[255 - 8 * lane - j];
+        sum += c[j];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - sum;
+      if (run < kk && kk <= incl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= kk) {
+            sm.scratch[64] = 255 - 8 * lane - j;
+            sm.scratch[65] = kk - run;
+            break;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm.scratch[64] << shift;
+    pmask |= 255u << shift;
+    kk = sm.scratch[65];
+    __syncthreads();
+  }
+  // take every key above the threshold and the first kk equal to it
+  int taken_eq = 0;
+  for (int base = 0; base < L; base += kIdxThreads) {
+    const int i = base + tid;
+    uint32_t key = 0;
+    if (i < L) key = key_at(i);
+    const bool gt = i < L && key != 0u && key > prefix;
+    const bool eq = i < L && key == prefix;
+    int tot;
+    const int before = block_exclusive_scan(eq ? 1 : 0, sm.scratch, tot);
+    const bool take = gt || (eq && taken_eq + before < kk);
+    const uint32_t word = __ballot_sync(0xffffffffu, take);
+    if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
+    taken_eq += tot;
+  }
+  __syncthreads();
+}
+
+struct IndexParams {
+  int B, Hkv;
+  const int32_t *seqlens;
+  const float *sd, *st;
+  int stride, n_sink, window, m_draft, budget;
+  int32_t *indices, *n_indices;
+  int *status;
+};
+
+__global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexParams p) {
+  extern __shared__ __align__(16) uint32_t ism[];
+  IdxSmem sm;
+  sm.bitmap = ism;
+  sm.hist = ism + kIdxBitmapWords;
+  sm.scratch = reinterpret_cast<int *>(sm.hist + 256);
+  sm.keys = reinterpret_cast<uint32_t *>(sm.scratch + 128);
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x / p.Hkv;
+  const int h = blockIdx.x % p.Hkv;
+  int L = __ldg(p.seqlens + b);
+  const int cap = min(p.stride, kIdxMaxL);
+  if (L < 0 || L > cap) {
+    record_status(p.status, VA_ERR_DEVICE_BOUNDS);
+    L = L < 0 ? 0 : cap;
+  }
+  const int nwords = (L + 31) / 32;
+  // fixed part: sinks [0, a) and window [wlo, L)
+  const int a = min(p.n_sink, L);
+  const int wlo = max(0, L - p.window);
+  for (int w = tid; w < nwords; w += kIdxThreads) {
+    uint32_t bits = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int i = 32 * w + j;
+      if (i < L && (i < a || i >= wlo)) bits |= 1u << j;
+    }
+    sm.bitmap[w] = bits;
+  }
+  __syncthreads();
+  const int fixed = a + (L - wlo) - max(0, a - wlo);
+  const int room = max(0, p.budget - fixed);
+  const int ncand = L - fixed;
+  const size_t row = ((size_t)b * p.Hkv + h);
+  const int m1 = max(0, min(min(p.m_draft, room), ncand));
+  select_top(p.sd + row * p.stride, L, m1, sm);
+  const int m2 = max(0, min(room - m1, ncand - m1));
+  select_top(p.st + row * p.stride, L, m2, sm);
+
+  // bitmap -> ascending positions
+  int32_t *out = p.indices + row * p.budget;
+  int written = 0;
+  for (int base = 0; base < nwords; base += kIdxThreads) {
+    const int w = base + tid;
+    const uint32_t bits = w < nwords ? sm.bitmap[w] : 0u;
+    int tot;
+    int off = written + block_exclusive_scan(__popc(bits), sm.scratch, tot);
+    uint32_t rem = bits;
+    while (rem) {
+      const int j = __ffs(rem) - 1;
+      rem &= rem - 1;
+      if (off < p.budget) out[off] = 32 * w + j;
+      ++off;
+    }
+    written += tot;
+  }
+  const int n = min(written, p.budget);
+  for (int i = n + tid; i < p.budget; i += kIdxThreads) out[i] = -1;
+  if (tid == 0) p.n_indices[row] = n;
+}
+
+size_t build_index_smem_bytes() {
+  return sizeof(uint32_t) * (kIdxBitmapWords + 256 + 128 + kIdxCacheKeys);
+}
+
+cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
+                               const float *score_target, int score_stride, int n_sink, int window, int m_draft,
+                               int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream) {
+  IndexParams p;
+  p.B = B;
+  p.Hkv = Hkv;
+  p.seqlens = seqlens;
+  p.sd = score_draft;
+  p.st = score_target;
+  p.stride = score_stride;
+  p.n_sink = n_sink;
+  p.window = window;
+  p.m_draft = m_draft;
+  p.budget = budget;
+  p.indices = indices;
+  p.n_indices = n_indices;
+  p.status = status;
+  const size_t smem = build_index_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(build_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  build_index_kernel<<<B * Hkv, kIdxThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self test: waits on an mbarrier nothing will ever complete;
+// the wait must give up after wait_ns and record VA_ERR_TIMEOUT.
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(int *status, uint64_t wait_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, wait_ns)) record_status(status, VA_ERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(int *status, uint64_t wait_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace va

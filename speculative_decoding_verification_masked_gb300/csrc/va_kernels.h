@@ -1,0 +1,60 @@
+// Internal interface between the C ABI layer (va_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "verify_attn.h"
+
+namespace va {
+
+// Everything one attention launch needs; plain values and device pointers.
+struct AttnParams {
+  // shape
+  int B, T, Hq, Hkv, D;
+  int R;       // packed query rows per (sequence, kv-head) = (Hq/Hkv) * T
+  int RG;      // 16-row groups per segment (1, 2 or 4)
+  int NRB;     // row blocks per (sequence, kv-head)
+  int S;       // segments = B * Hkv * NRB
+  int rows_pad;// rows per segment slot in the partial buffers
+  int use_tc;  // 1: tcgen05 kernel (bf16, D 128, more than 64 packed rows)
+  float scale;
+  va_dtype dtype;
+  int layout;  // va_layout
+  // inputs
+  const void *q, *k, *v;
+  int len_cap;  // dense/sparse: max_cache_len; paged: max_pages * page_size
+  int num_pages, page_shift, max_pages;
+  const int32_t *page_table;
+  const int32_t *seqlens;
+  const int32_t *indices, *n_indices;
+  int max_indices;
+  const int32_t *parent;
+  const uint32_t *mask;
+  int mask_words;
+  // outputs
+  void *out;
+  float *lse;
+  // workspace
+  int *status;
+  int2 *meta;
+  float *lse_part, *o_part;
+  uint64_t wait_ns;
+};
+
+size_t attn_smem_required(const AttnParams &p);
+size_t attn_tc_smem_required(const AttnParams &p);
+cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                             cudaStream_t stream);
+cudaError_t launch_combine_generic(int n_rows, int n_parts, int D, const float *o_parts, const float *lse_parts,
+                                   va_dtype out_dtype, void *out, float *lse, cudaStream_t stream);
+cudaError_t launch_tree_mask(int B, int T, const int32_t *parent, uint32_t *mask, int *status, cudaStream_t stream);
+cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
+                               const float *score_target, int score_stride, int n_sink, int window, int m_draft,
+                               int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int *status, uint64_t wait_ns, cudaStream_t stream);
+
+}  // namespace va

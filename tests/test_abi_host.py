@@ -1,0 +1,93 @@
+"""Host-only checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every symbol the headers declare, and rejects bad
+arguments with the documented status before touching any device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_masked_gb300 as va
+from speculative_decoding_verification_masked_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#")):
+                names.add(m.group(1))
+    return names
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    L = api.lib()
+    names = _declared_functions()
+    assert {"verify_attn_dense", "verify_attn_paged", "verify_attn_sparse", "verify_attn_combine",
+            "verify_tree_mask_from_parents", "verify_build_index", "verify_attn_workspace_size",
+            "verify_attn_check_status"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+    assert va.version().endswith("sm_103a")
+
+
+FAKE = 1 << 20  # a non-NULL address validation never dereferences
+
+
+def _shape(**kw):
+    d = dict(B=1, T=8, Hq=32, Hkv=8, D=128, dtype=0, scale=0.088)
+    d.update(kw)
+    return api.VaShape(d["B"], d["T"], d["Hq"], d["Hkv"], d["D"], d["dtype"], d["scale"])
+
+
+def _dense(shape, parent=None, mask=None, ws=FAKE, q=FAKE, max_len=100):
+    L = api.lib()
+    return L.verify_attn_dense(ctypes.byref(shape) if shape is not None else None, q, FAKE, FAKE, max_len, FAKE,
+                               parent, mask, None, FAKE, FAKE, ws, 1 << 30, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), api.VA_ERR_INVALID_ARG),
+    (dict(Hq=30), api.VA_ERR_INVALID_ARG),
+    (dict(dtype=7), api.VA_ERR_INVALID_ARG),
+    (dict(scale=0.0), api.VA_ERR_INVALID_ARG),
+    (dict(T=65), api.VA_ERR_UNSUPPORTED),
+    (dict(D=96), api.VA_ERR_UNSUPPORTED),
+    (dict(dtype=2, D=128), api.VA_ERR_UNSUPPORTED),
+    (dict(B=300, Hkv=8), api.VA_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_rejected_on_host(kw, code):
+    assert _dense(_shape(**kw)) == code
+    assert api.lib().verify_attn_last_error()
+
+
+def test_bad_pointers_rejected_on_host():
+    assert _dense(None) == api.VA_ERR_INVALID_ARG
+    assert _dense(_shape(), q=None) == api.VA_ERR_INVALID_ARG
+    assert _dense(_shape(), parent=FAKE, mask=FAKE) == api.VA_ERR_INVALID_ARG
+    assert _dense(_shape(), ws=None) == api.VA_ERR_WORKSPACE
+    assert _dense(_shape(), ws=FAKE + 16) == api.VA_ERR_WORKSPACE
+    assert _dense(_shape(), q=FAKE + 4) == api.VA_ERR_INVALID_ARG
+    assert _dense(_shape(), max_len=3) == api.VA_ERR_INVALID_ARG
+
+
+def test_paged_sparse_index_mask_combine_argument_checks():
+    L = api.lib()
+    s = _shape()
+    bad_page = L.verify_attn_paged(ctypes.byref(s), FAKE, FAKE, FAKE, 10, 12, FAKE, 4, FAKE, None, None, None, FAKE,
+                                   FAKE, FAKE, 1 << 30, None)
+    assert bad_page == api.VA_ERR_INVALID_ARG
+    no_idx = L.verify_attn_sparse(ctypes.byref(s), FAKE, FAKE, FAKE, 100, FAKE, None, FAKE, 16, None, None, None,
+                                  FAKE, FAKE, FAKE, 1 << 30, None)
+    assert no_idx == api.VA_ERR_INVALID_ARG
+    assert L.verify_build_index(1, 1, FAKE, FAKE, FAKE, 100, 4, 256, 10, 200, FAKE, FAKE, None, None) == \
+        api.VA_ERR_INVALID_ARG  # budget < sinks + window
+    assert L.verify_tree_mask_from_parents(1, 65, FAKE, FAKE, None, None) == api.VA_ERR_UNSUPPORTED
+    assert L.verify_attn_combine(4, 0, 128, FAKE, FAKE, 0, FAKE, FAKE, None) == api.VA_ERR_INVALID_ARG
+    assert L.verify_attn_combine(4, 2, 96, FAKE, FAKE, 0, FAKE, FAKE, None) == api.VA_ERR_UNSUPPORTED
+    assert L.verify_attn_workspace_size(None) == 0

@@ -1,0 +1,276 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded inputs.
+
+Bars: bf16 (and fp32) outputs max-abs <= 2e-3, lse max-abs <= 1e-3, masks and
+verify index sets bit-exact.  Small cases span several 64-key tiles with a
+ragged tail; the full-size workloads are checked on every row the oracle can
+afford (all of them for chain / sparse / paged, one kv-head group for tree).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_masked_gb300 as va
+import workloads as W
+from tests.gpu_util import compare, dev_i32, dev_words, run_library
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, skipped there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    va.api.lib()
+
+
+# ----------------------------------------------------------------------------
+# a1: tree -> bitmask
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [1, 5, 8, 31, 32, 33, 63, 64])
+def test_tree_mask_bit_exact(T):
+    rng = np.random.default_rng(T)
+    parents = np.stack([W.random_parents(T, rng) for _ in range(7)])
+    if T >= 8:
+        parents[3] = W.depth_tree_parents(T, 6, rng)[0] if T >= 7 else parents[3]
+    parents[0] = W.chain_parents(T)
+    got = va.verify_tree_mask_from_parents(dev_i32(parents)).cpu().numpy().view(np.uint32)
+    want = oracle.tree_mask_words(parents)
+    assert np.array_equal(got, want)
+
+
+def test_tree_mask_bad_parent_is_reported():
+    ws = va.Workspace(256)
+    parents = np.array([[-1, 0, 5, 1]], np.int32)  # parent[2] = 5 is not earlier
+    va.verify_tree_mask_from_parents(dev_i32(parents), workspace=ws)
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(ws)
+    assert ei.value.status == va.api.VA_ERR_DEVICE_BOUNDS
+    va.verify_attn_check_status(ws)  # cleared
+
+
+# ----------------------------------------------------------------------------
+# a2-a4: attention, small cases
+# ----------------------------------------------------------------------------
+
+def _check(w, mode="parent", **kw):
+    ref = oracle.verify(w)
+    out, lse = run_library(w, mode=mode, **kw)
+    torch.cuda.synchronize()
+    return compare(out, lse, ref)
+
+
+def test_tiny_config_full():
+    w = W.make_workload("tiny")
+    for mode in ("parent", "mask"):
+        eo, el, _ = _check(w, mode)
+        assert eo < 1e-4 and el < 1e-4  # fp32 path, no TF32
+
+
+@pytest.mark.parametrize("L", [0, 1, 63, 64, 1000, 4099])
+def test_chain_small(L):
+    w = W.make_workload("chain", seed=L, L=L)
+    for mode in ("parent", "causal", "mask"):
+        _check(w, mode)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tree_small(seed):
+    w = W.make_workload("tree", seed=seed, L=3001)
+    for mode in ("parent", "mask"):
+        _check(w, mode)
+
+
+@pytest.mark.parametrize("Hq,Hkv,T,D", [(8, 8, 3, 128), (16, 2, 8, 128), (32, 8, 5, 64), (4, 1, 64, 64),
+                                        (12, 4, 7, 128), (32, 2, 9, 128), (32, 4, 16, 128), (20, 2, 10, 128),
+                                        (32, 8, 64, 128), (16, 1, 40, 128)])
+def test_shapes_and_row_blocks(Hq, Hkv, T, D):
+    """group*T from 3 to 640 rows: the mma.sync kernel with 1, 2, 4 row groups and
+    several row blocks, and the tcgen05 kernel with one or two 128-row M-tiles,
+    padded rows and several 256-row blocks."""
+    w = W.make_workload("tree", seed=Hq * T, Hq=Hq, Hkv=Hkv, T=T, D=D, L=517, tree="random", B=2)
+    _check(w, "parent")
+
+
+def test_random_masks_and_empty_rows():
+    """Arbitrary bitmasks; with L=0 a row that hides itself sees nothing (out 0, lse -inf)."""
+    w = W.make_workload("tree", seed=9, B=3, T=19, L=130, tree="random_mask", density=0.3)
+    _check(w, "mask")
+    w0 = W.make_workload("tree", seed=10, B=2, T=12, L=0, tree="random_mask", density=0.3)
+    m = w0.mask_words.copy()
+    m[0, 5, 0] = 0  # row 5 of sequence 0 sees no key at all
+    w0.mask_words = m
+    ref = oracle.verify(w0)
+    assert np.isneginf(ref["lse"][0, :, 5]).all()
+    out, lse = run_library(w0, "mask")
+    compare(out, lse, ref)
+    assert torch.all(out[0, 5] == 0)
+
+
+@pytest.mark.parametrize("page_size", [1, 16, 64])
+def test_paged_small(page_size):
+    w = W.make_workload("paged", seed=page_size, B=5, L_lo=3, L_hi=700, page_size=page_size, spare_pages=7)
+    _check(w, "mask")
+    wb = W.make_workload("paged", seed=page_size + 1, B=4, L_lo=40, L_hi=300, page_size=page_size,
+                         tree="block_isolated")
+    _check(wb, "mask")
+    wt = W.make_workload("paged", seed=page_size + 2, B=3, L_lo=40, L_hi=300, page_size=page_size,
+                         tree="depth", T=16, depth=4)
+    _check(wt, "parent")
+
+
+def test_sparse_small_with_library_indices():
+    w = W.make_workload("sparse", seed=3, B=3, L_lo=200, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60)
+    ref = oracle.verify(w)
+    idx, cnt = va.verify_build_index(dev_i32(w.seqlens), torch.from_numpy(w.score_draft).cuda(),
+                                     torch.from_numpy(w.score_target).cuda(), w.n_sink, w.window, w.m_draft,
+                                     w.budget)
+    assert np.array_equal(cnt.cpu().numpy(), ref["n_indices"])
+    assert np.array_equal(idx.cpu().numpy(), ref["indices"])
+    out, lse = run_library(w, "parent", indices=idx, n_indices=cnt)
+    compare(out, lse, ref)
+
+
+def test_sparse_full_index_equals_dense_on_gpu():
+    w = W.make_workload("sparse", seed=4, B=2, L_lo=100, L_hi=300, budget=512, window=8, n_sink=2, m_draft=3)
+    Lmax = int(w.seqlens.max())
+    idx = np.full((w.B, w.Hkv, Lmax), -1, np.int32)
+    cnt = np.zeros((w.B, w.Hkv), np.int32)
+    for b in range(w.B):
+        idx[b, :, : w.seqlens[b]] = np.arange(w.seqlens[b])
+        cnt[b] = w.seqlens[b]
+    out_s, lse_s = run_library(w, "parent", indices=dev_i32(idx), n_indices=dev_i32(cnt))
+    w.layout = "dense"
+    out_d, lse_d = run_library(w, "parent")
+    ref = oracle.verify(w)
+    compare(out_s, lse_s, ref)
+    compare(out_d, lse_d, ref)
+
+
+# ----------------------------------------------------------------------------
+# verify index set (a5)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L_lo,L_hi", [(1, 300), (2000, 5000), (40000, 50000)])
+def test_build_index_bit_exact(L_lo, L_hi):
+    """Includes L below the budget, ties (coarse scores) and L past the shared-memory cache."""
+    rng = np.random.default_rng(L_hi)
+    B, Hkv = 4, 3
+    seqlens = rng.integers(L_lo, L_hi + 1, size=B).astype(np.int32)
+    stride = int(seqlens.max()) + 5
+    sd = (rng.integers(0, 50, size=(B, Hkv, stride)) / 49).astype(np.float32)
+    st = rng.random((B, Hkv, stride), dtype=np.float32)
+    st[0, 0, :10] = -0.0
+    st[0, 0, 10:20] = 0.0
+    sd[1, 1, :] = np.float32(0.5)  # all ties
+    args = (4, 64, 300, 1024)
+    ref_idx, ref_n = oracle.build_verify_index(sd, st, seqlens, *args)
+    idx, n = va.verify_build_index(dev_i32(seqlens), torch.from_numpy(sd).cuda(), torch.from_numpy(st).cuda(), *args)
+    assert np.array_equal(n.cpu().numpy(), ref_n)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+# ----------------------------------------------------------------------------
+# combine (exposed merge)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_combine_matches_oracle_merge(D):
+    rng = np.random.default_rng(D)
+    S, R = 7, 33
+    o = rng.standard_normal((S, R, D)).astype(np.float32)
+    l = (rng.standard_normal((S, R)) * 3).astype(np.float32)
+    l[2, :5] = -np.inf
+    l[:, 7] = -np.inf  # a row with every part empty
+    ro, rl = oracle.lse_merge(o.astype(np.float64), l.astype(np.float64))
+    out, lse = va.verify_attn_combine(torch.from_numpy(o).cuda(), torch.from_numpy(l).cuda())
+    out = out.cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert np.isneginf(lse[7]) and np.all(out[7] == 0)
+    fin = np.isfinite(rl)
+    assert np.abs(out - ro).max() < 1e-5
+    assert np.abs(lse[fin] - rl[fin]).max() < 1e-5
+
+
+# ----------------------------------------------------------------------------
+# errors recorded on the device, bounded waits, determinism
+# ----------------------------------------------------------------------------
+
+def test_device_bounds_are_reported_not_faulted():
+    w = W.make_workload("paged", seed=5, B=3, L_lo=100, L_hi=200)
+    table = w.page_table.copy()
+    table[1, 2] = 10 ** 6  # page out of range: clamped, recorded
+    shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0)
+    ws = va.Workspace.for_shape(shape)
+    va.verify_attn_paged(w.q.cuda(), w.k_pages.cuda(), w.v_pages.cuda(), dev_i32(table), dev_i32(w.seqlens),
+                         tree_mask=dev_words(w.mask_words), workspace=ws)
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(ws)
+    assert ei.value.status == va.api.VA_ERR_DEVICE_BOUNDS
+    # a seqlen past the cache is clamped and recorded too
+    wd = W.make_workload("chain", seed=6, L=300)
+    sl = wd.seqlens.copy()
+    sl[0] = wd.max_cache_len
+    shape = va.make_shape(1, wd.T, wd.Hq, wd.Hkv, wd.D, 0)
+    ws2 = va.Workspace.for_shape(shape)
+    va.verify_attn_dense(wd.q.cuda(), wd.k_cache.cuda(), wd.v_cache.cuda(), dev_i32(sl), workspace=ws2)
+    with pytest.raises(va.VerifyAttnError):
+        va.verify_attn_check_status(ws2)
+    # the workspace is usable again afterwards
+    out, lse = run_library(wd, "parent", workspace=ws2)
+    va.verify_attn_check_status(ws2)
+    compare(out, lse, oracle.verify(wd))
+
+
+def test_bounded_wait_times_out_cleanly():
+    ws = va.Workspace(256)
+    st = va.api.lib().verify_attn_selftest_wait_timeout(ws.ptr, 2_000_000, va.api._stream())
+    assert st == 0
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(ws)
+    assert ei.value.status == va.api.VA_ERR_TIMEOUT
+    va.verify_attn_check_status(ws)
+
+
+def test_deterministic_and_workspace_reuse():
+    w = W.make_workload("chain", seed=7, L=5000)
+    shape = va.make_shape(1, w.T, w.Hq, w.Hkv, w.D, 0)
+    ws = va.Workspace.for_shape(shape)
+    o1, l1 = run_library(w, "parent", workspace=ws)
+    o2, l2 = run_library(w, "parent", workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    va.verify_attn_check_status(ws)
+
+
+def test_workspace_too_small_is_rejected():
+    w = W.make_workload("chain", seed=8, L=100)
+    small = va.Workspace(1024)
+    with pytest.raises(va.VerifyAttnError) as ei:
+        run_library(w, "parent", workspace=small)
+    assert ei.value.status == va.api.VA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("case", ["sparse", "paged_isolated", "dense_ragged"])
+def test_partials_never_read_stale_workspace(case):
+    """Ragged lengths with fewer 64-key tiles than CTAs: every partial slot the
+    combine reads must have been written by this very call.  The workspace is
+    filled with NaN bytes first, so reading a stale slot cannot go unnoticed."""
+    if case == "sparse":
+        w = W.make_workload("sparse", seed=3, B=3, L_lo=200, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60)
+    elif case == "paged_isolated":
+        w = W.make_workload("paged", seed=17, B=4, L_lo=40, L_hi=300, page_size=16, tree="block_isolated")
+    else:
+        w = W.make_workload("tree", seed=4, B=5, L_lo=1, L_hi=200, T=9, tree="random")
+    ref = oracle.verify(w)
+    shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0)
+    ws = va.Workspace.for_shape(shape)
+    ws.buffer.fill_(0xFF)
+    assert va.api.lib().verify_attn_workspace_init(ws.ptr, ws.nbytes, va.api._stream()) == 0
+    kw = {}
+    if w.layout == "sparse":
+        kw = dict(indices=dev_i32(ref["indices"]), n_indices=dev_i32(ref["n_indices"]))
+    out, lse = run_library(w, "mask" if w.parent is None else "parent", workspace=ws, **kw)
+    va.verify_attn_check_status(ws)
+    compare(out, lse, ref)

@@ -221,7 +221,7 @@ class Workload:
         """
         per_key = self.D * 2 * self.elem_bytes
         if self.layout == "sparse":
-            n_prefix = self.B * self.Hkv * self.budget_effective_total()
+            n_prefix = self.Hkv * self.budget_effective_total()
         else:
             n_prefix = int(self.seqlens.astype(np.int64).sum()) * self.Hkv
         return (n_prefix + self.B * self.Hkv * self.T) * per_key
