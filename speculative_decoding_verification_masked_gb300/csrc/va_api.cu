@@ -108,8 +108,6 @@ struct RowPlan {
   int R, RG, NRB, rows_pad, S, use_tc;
 };
 
-constexpr bool kTcValidated = false;  // tcgen05 path not yet validated on hardware
-
 // Kernel choice and row blocking.  More than 64 packed rows (bf16, D 128) go to
 // the tcgen05 kernel in blocks of up to 256 rows (two 128-row M-tiles); the
 // rest to the mma.sync kernel in blocks of 16, 32 or 64 rows.
@@ -120,7 +118,7 @@ RowPlan row_plan(const va_shape &s) {
   if (s.dtype == VA_DTYPE_FP32) {
     r.RG = 4;
     r.rows_pad = 64;
-  } else if (kTcValidated && s.D == 128 && r.R > 64) {
+  } else if (s.D == 128 && r.R > 64) {
     r.use_tc = 1;
     r.RG = 4;
     r.rows_pad = r.R > 128 ? 256 : 128;
