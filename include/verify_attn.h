@@ -115,6 +115,38 @@ va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_
                             size_t ws_bytes, va_stream stream);
 
 /*
+ * verify_attn_dense for callers that cannot allocate device memory: the same
+ * computation and arguments, but no workspace.  Meant for code that is handed
+ * only its input and output buffers (for example a plugin inside a host
+ * framework that owns the device allocator) and for deployments that fix their
+ * device memory at start-up and allow no allocation afterwards.  The papers
+ * have no counterpart: this is an interface convenience, not part of the method.
+ *
+ * Scratch.  The partial results, segment bookkeeping and status word live in
+ * one file-scope device array of 8 MiB that every GPU which loads this library
+ * holds until the process exits.  The first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress, with the device current); make
+ * that first call before any stream capture.  No call allocates or frees
+ * memory.  A shape whose scratch exceeds 8 MiB (verify_attn_workspace_size) is
+ * rejected with VA_ERR_UNSUPPORTED before anything is enqueued.  On a 152-SM
+ * GPU, d 128 and at most 32 packed query rows per kv-head (GQA group x T),
+ * about 350 (sequence, kv-head) pairs fit -- e.g. one sequence with 8 draft
+ * tokens, or 16 sequences of 5; a batch of 64 sequences of 16 does not.
+ * Sharing.  Every call uses the same array and leaves its contents behind;
+ * each call clears the status word it needs.  Calls whose work overlaps on the
+ * GPU (different streams, or different host threads) race on the array and
+ * give undefined results: serialise them.
+ * device_status (may be NULL): a caller-owned device int32 that receives this
+ * call's device status word (VA_OK or the first device-side error), copied on
+ * `stream` after the computation.
+ */
+va_status verify_attn_dense_noalloc(const va_shape *shape, const void *q, const void *k_cache,
+                                    const void *v_cache, int max_cache_len, const int32_t *seqlens,
+                                    const int32_t *tree_parent, const uint32_t *tree_mask,
+                                    const int32_t *positions, void *out, float *lse,
+                                    int32_t *device_status, va_stream stream);
+
+/*
  * Verification attention over a paged cache (HiSpec section 2: paged attention
  * with block tables, so each sequence of a batch can accept a different
  * number of tokens without padding).  Logical slot p of sequence b lives at

@@ -56,6 +56,7 @@ _SIGS = {
     "verify_attn_last_error": (ctypes.c_char_p, []),
     "verify_attn_version": (ctypes.c_char_p, []),
     "verify_attn_selftest_wait_timeout": (_I, [_P, ctypes.c_ulonglong, _P]),
+    "verify_attn_dense_noalloc": (_I, [ctypes.POINTER(VaShape), _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -174,6 +175,19 @@ def verify_attn_dense(q, k_cache, v_cache, seqlens, tree_parent=None, tree_mask=
     _check(lib().verify_attn_dense(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[1],
                                    _ptr(seqlens), _ptr(tree_parent), _ptr(tree_mask), _ptr(positions), _ptr(out),
                                    _ptr(lse), ws.ptr, ws.nbytes, _stream(stream)))
+    return out, lse
+
+
+def verify_attn_dense_noalloc(q, k_cache, v_cache, seqlens, tree_parent=None, tree_mask=None, positions=None,
+                              out=None, lse=None, device_status=None, scale=None, stream=None):
+    """verify_attn_dense without a workspace (fixed 8 MiB static device scratch inside
+    the library) for callers that cannot allocate; see include/verify_attn.h."""
+    shape = _shape_of(q, k_cache.shape[2], scale)
+    out, lse = _outputs(q, out, lse)
+    _check(lib().verify_attn_dense_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           k_cache.shape[1], _ptr(seqlens), _ptr(tree_parent), _ptr(tree_mask),
+                                           _ptr(positions), _ptr(out), _ptr(lse), _ptr(device_status),
+                                           _stream(stream)))
     return out, lse
 
 

@@ -416,3 +416,71 @@ va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point that allocates nothing (declared in verify_attn.h).
+//
+// Some callers cannot hand the library a workspace: a plugin that is given only
+// its input and output tensors by a host framework and has no handle on that
+// framework's device allocator, or a deployment that fixes its device memory at
+// start-up and forbids any allocation afterwards.  For them the scratch this
+// call needs (partial results, segment bookkeeping, the device status word)
+// lives in one file-scope device array of fixed size, which every GPU that
+// loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_static_mu;
+void *g_static_addr[64] = {nullptr};  // device address of g_static_scratch, per device
+
+// Resolve the device address of the static scratch for the current device
+// (once per device, with that device current).  In host code the array's name
+// is only a host-side stand-in, so kernels must receive this address instead.
+va_status static_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(VA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_addr[dev] = ptr;
+  }
+  *out = g_static_addr[dev];
+  return VA_OK;
+}
+}  // namespace
+
+extern "C" va_status verify_attn_dense_noalloc(const va_shape *shape, const void *q, const void *k_cache,
+                                               const void *v_cache, int max_cache_len, const int32_t *seqlens,
+                                               const int32_t *tree_parent, const uint32_t *tree_mask,
+                                               const int32_t *positions, void *out, float *lse,
+                                               int32_t *device_status, va_stream stream) {
+  va_status st = check_shape(shape);
+  if (st != VA_OK) return st;
+  const size_t need = verify_attn_workspace_size(shape);
+  if (need == 0) return fail(VA_ERR_CUDA, "no usable CUDA device");
+  if (need > kStaticScratchBytes)
+    return fail(VA_ERR_UNSUPPORTED,
+                "this shape needs %zu bytes of scratch; the static scratch of verify_attn_dense_noalloc holds %zu "
+                "bytes -- use verify_attn_dense with a caller workspace",
+                need, kStaticScratchBytes);
+  void *scratch = nullptr;
+  st = static_scratch_address(&scratch);
+  if (st != VA_OK) return st;
+  // the status word must start at zero for this call's device-side checks
+  cudaError_t e = cudaMemsetAsync(scratch, 0, va::kHeaderBytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch status word");
+  st = verify_attn_dense(shape, q, k_cache, v_cache, max_cache_len, seqlens, tree_parent, tree_mask, positions, out,
+                         lse, scratch, kStaticScratchBytes, stream);
+  if (st != VA_OK) return st;
+  if (device_status != nullptr) {
+    e = cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the device status word");
+  }
+  return ok();
+}
