@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float pv = exp2f(fmaf(sacc[nt][e], cl2, -mu[e >> 1]));
+              const float pv = ex2_approx(fmaf(sacc[nt][e], cl2, -mu[e >> 1]));
               sacc[nt][e] = pv;
               ls[e >> 1] += pv;
             }

@@ -264,7 +264,6 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const int lt0 = max(tstart[s], t0) - tstart[s];
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoftThreads + 32);  // Q of this segment is in shared memory
-      // prologue: S of the first tile
       acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
       for (int i = 0; i < NMT; ++i) issue_s(i, jt & 1, it % NS);
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
@@ -273,14 +272,18 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         const uint32_t pph = (uint32_t)(jt >> 1) & 1u;
         const bool has_next = lt + 1 < lt1;
         const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
-        const int st_n = (it + 1) % NS;
+        // M-tiles in turn: PV_i(lt), then -- once it has completed -- S_i(lt+1), so
+        // each warpgroup's softmax overlaps the other M-tile's MMAs and no MMA of
+        // an M-tile runs while that M-tile's softmax reads or writes TMEM
         for (int i = 0; i < NMT; ++i) {
           wait_ok(p_full + 2 * i + b, pph);
           issue_pv(i, b, st, lt == lt0, exact);
-          if (i == NMT - 1 && ok && lane == 0) umma_commit(empty + st);  // K/V of this tile no longer needed
+          wait_ok(o_done + i, (uint32_t)jt & 1u);
+          tc_fence_after();
+          if (i == NMT - 1 && lane == 0) mbar_arrive(empty + st);  // every PV of this tile is done
           if (has_next) {
-            if (i == 0) acquire_stage(st_n, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
-            issue_s(i, b ^ 1, st_n);
+            if (i == 0) acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
+            issue_s(i, b ^ 1, (it + 1) % NS);
           }
         }
       }
@@ -380,9 +383,16 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           if (!vis) sv[j] = -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      float mx;
+      {  // pairwise max: short dependency chains
+        float m8[8];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
+        for (int q = 0; q < 8; ++q) {
+          m8[q] = fmaxf(fmaxf(fmaxf(sv[8 * q], sv[8 * q + 1]), fmaxf(sv[8 * q + 2], sv[8 * q + 3])),
+                        fmaxf(fmaxf(sv[8 * q + 4], sv[8 * q + 5]), fmaxf(sv[8 * q + 6], sv[8 * q + 7])));
+        }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      }
       const float m_new = fmaxf(m_used, mx);
       if (lt == lt0) {
         m_used = m_new;
@@ -410,18 +420,32 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         }
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
-      uint32_t ph[32], pl[32];
-      float ls = 0.f;
+      uint32_t ph[32];
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short add chains
+      if (masked) {
+        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts)
+        uint32_t pl[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float a = exp2f(fmaf(sv[2 * j], cl2, -mu));
-        const float bq = exp2f(fmaf(sv[2 * j + 1], cl2, -mu));
-        ls += a + bq;
-        split_bf16x2(a, bq, ph[j], pl[j]);
+        for (int j = 0; j < 32; ++j) {
+          const float a = ex2_approx(fmaf(sv[2 * j], cl2, -mu));
+          const float bq = ex2_approx(fmaf(sv[2 * j + 1], cl2, -mu));
+          ls4[j & 3] += a + bq;
+          split_bf16x2(a, bq, ph[j], pl[j]);
+        }
+        tmem_st32(tS, ph);
+        tmem_st32(tS + 32, pl);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float a = ex2_approx(fmaf(sv[2 * j], cl2, -mu));
+          const float bq = ex2_approx(fmaf(sv[2 * j + 1], cl2, -mu));
+          ls4[j & 3] += a + bq;
+          ph[j] = pack_bf16(a, bq);
+        }
+        tmem_st32(tS, ph);
       }
+      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l += ls;
-      tmem_st32(tS, ph);
-      if (masked) tmem_st32(tS + 32, pl);  // lo parts feed a second MMA on draft tiles
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full + 2 * mi + b);

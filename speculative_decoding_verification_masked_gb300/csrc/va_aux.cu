@@ -98,6 +98,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int &to
 
 // Select the k largest keys among positions [0, L) not yet in the bitmap and
 // add them to it.  k must not exceed the number of such positions.
+//
+// Radix select, most significant digit first.  After each 8-bit digit the
+// bucket holding the k-th largest key is known together with how many keys
+// above it are already certain.  If that bucket holds exactly the keys still
+// needed, every key at or above it is taken and the search stops (the usual
+// case for continuous scores).  Otherwise the search narrows to the bucket; if
+// keys equal to the final threshold still outnumber the quota, they are taken
+// in increasing position order (the tie rule).
 __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
   if (k <= 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,7 +122,9 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
 
   uint32_t prefix = 0, pmask = 0;
   int kk = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  int shift = 24;
+  bool exact_bucket = false;
+  for (; shift >= 0; shift -= 8) {
     if (tid < 256) sm.hist[tid] = 0;
     __syncthreads();
     for (int base = 0; base < L; base += kIdxThreads) {
@@ -152,6 +162,7 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
           if (run + c[j] >= kk) {
             sm.scratch[64] = 255 - 8 * lane - j;
             sm.scratch[65] = kk - run;
+            sm.scratch[66] = (run + c[j] == kk) ? 1 : 0;  // the bucket is taken whole
             break;
           }
           run += c[j];
@@ -162,9 +173,27 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
     prefix |= (uint32_t)sm.scratch[64] << shift;
     pmask |= 255u << shift;
     kk = sm.scratch[65];
+    exact_bucket = sm.scratch[66] != 0;
     __syncthreads();
+    if (exact_bucket) break;
   }
-  // take every key above the threshold and the first kk equal to it
+  if (exact_bucket) {
+    // every key whose digits down to `shift` are >= the chosen prefix is taken
+    for (int base = 0; base < L; base += kIdxThreads) {
+      const int i = base + tid;
+      bool take = false;
+      if (i < L) {
+        const uint32_t key = key_at(i);
+        take = key != 0u && (key & pmask) >= prefix;
+      }
+      const uint32_t word = __ballot_sync(0xffffffffu, take);
+      if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
+    }
+    __syncthreads();
+    return;
+  }
+  // ties at the full 32-bit threshold exceed the quota: above-threshold keys plus
+  // the first kk equal keys in position order
   int taken_eq = 0;
   for (int base = 0; base < L; base += kIdxThreads) {
     const int i = base + tid;

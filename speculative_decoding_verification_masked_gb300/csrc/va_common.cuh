@@ -167,6 +167,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^x by the PTX approximate base-2 exponential (flushes subnormal results to
+// zero; relative error ~2^-22, far below the bf16 rounding P gets afterwards).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Split two fp32 values into bf16 hi and lo parts (x ~= hi + lo to ~2^-16
 // relative), packed as bf16x2 registers for an mma A operand.
 __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uint32_t &lo) {
