@@ -105,7 +105,7 @@ int device_sm_count(int *dev_out) {
 
 // Row blocking of the packed (group * T) query rows of one kv-head.
 struct RowPlan {
-  int R, RG, NRB, rows_pad, S, use_tc;
+  int R, RG, NRB, rows_pad, S, use_tc, cps;
 };
 
 // Kernel choice and row blocking.  More than 64 packed rows (bf16, D 128) go to
@@ -128,6 +128,8 @@ RowPlan row_plan(const va_shape &s) {
   }
   r.NRB = (r.R + r.rows_pad - 1) / r.rows_pad;
   r.S = s.B * s.Hkv * r.NRB;
+  // two CTAs per SM for the mma.sync kernel with small per-warp state
+  r.cps = (!r.use_tc && s.dtype == VA_DTYPE_BF16 && r.RG <= 2) ? 2 : 1;
   return r;
 }
 
@@ -153,7 +155,7 @@ va_status check_shape(const va_shape *s) {
 
 size_t workspace_bytes(const va_shape &s, int sm_count) {
   const RowPlan rp = row_plan(s);
-  const int slots = rp.S + sm_count;
+  const int slots = rp.S + rp.cps * sm_count;  // one partial slot per (segment, CTA) boundary
   return va::ws_layout(rp.S, slots, rp.rows_pad, s.D).total;
 }
 
@@ -209,6 +211,7 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.S = rp.S;
   p.rows_pad = rp.rows_pad;
   p.use_tc = rp.use_tc;
+  p.cps = rp.cps;
   p.scale = s.scale;
   p.dtype = s.dtype;
   p.layout = layout;
@@ -230,7 +233,7 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.mask_words = (s.T + 31) / 32;
   p.out = c.out;
   p.lse = c.lse;
-  const va::WsLayout wl = va::ws_layout(rp.S, rp.S + sms, rp.rows_pad, s.D);
+  const va::WsLayout wl = va::ws_layout(rp.S, rp.S + rp.cps * sms, rp.rows_pad, s.D);
   uint8_t *ws = static_cast<uint8_t *>(c.ws);
   p.status = reinterpret_cast<int *>(ws);
   p.meta = reinterpret_cast<int2 *>(ws + wl.meta_off);
@@ -242,7 +245,8 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
   const long long tiles_cap = (long long)rp.S * ((keys_cap + 63) / 64);
   if (tiles_cap >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "problem too large (%lld key tiles)", tiles_cap);
-  const int grid = (int)(tiles_cap < sms ? tiles_cap : sms);
+  const long long ctas = (long long)rp.cps * sms;
+  const int grid = (int)(tiles_cap < ctas ? tiles_cap : ctas);
   if (va::attn_smem_required(p) > 232448) return fail(VA_ERR_UNSUPPORTED, "shared memory plan too large");
   CUtensorMap tmk, tmv;
   memset(&tmk, 0, sizeof tmk);

@@ -42,10 +42,13 @@ namespace va {
 constexpr int kNWC = 4;  // consumer warps
 constexpr int kThreads = (kNWC + 1) * 32;
 
-template <typename Tin, int D>
+// CPS = CTAs resident per SM: 2 when a consumer warp's state is small enough
+// (at most 32 packed rows), so two CTAs interleave their latency-bound warps;
+// each then keeps a shorter ring (the SM as a whole still has 128 KB in flight).
+template <typename Tin, int D, int CPS = 1>
 struct Cfg : StageGeom<Tin, D> {
   using G = StageGeom<Tin, D>;
-  static constexpr int kStages = (G::kStageBytes <= 16384) ? 8 : 5;
+  static constexpr int kStages = CPS == 2 ? (G::kStageBytes <= 16384 ? 4 : 2) : ((G::kStageBytes <= 16384) ? 8 : 5);
   static constexpr bool kF32 = std::is_same<Tin, float>::value;
   static constexpr int kMergeBytes = kF32 ? 128 * (64 + 2) * 4 : kNWC * 16 * (D * 4 + 8);
 };
@@ -54,11 +57,11 @@ struct Cfg : StageGeom<Tin, D> {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <typename Tin, int D, int RG>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename Tin, int D, int RG, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
     verify_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
-  using C = Cfg<Tin, D>;
+  using C = Cfg<Tin, D, CPS>;
   constexpr int NS = C::kStages;
   constexpr int KW = C::kF32 ? 2 : kNWC / RG;  // key-split warps per row group
   constexpr int RPS = C::kF32 ? 64 : 16 * RG;  // packed rows per segment
@@ -619,18 +622,18 @@ __global__ void __launch_bounds__(128) combine_generic_kernel(int n_rows, int n_
 // ---------------------------------------------------------------------------
 // host-side launch helpers
 // ---------------------------------------------------------------------------
-template <typename Tin, int D, int RG>
+template <typename Tin, int D, int RG, int CPS>
 static size_t attn_smem_bytes(int S) {
-  using C = Cfg<Tin, D>;
+  using C = Cfg<Tin, D, CPS>;
   return 1024 + (size_t)C::kStages * C::kStageBytes + C::kMergeBytes + 2 * C::kStages * 8 + 16 +
          (size_t)(S + 1) * 4;
 }
 
-template <typename Tin, int D, int RG>
+template <typename Tin, int D, int RG, int CPS = 1>
 static cudaError_t launch_attn_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream) {
-  const size_t smem = attn_smem_bytes<Tin, D, RG>(p.S);
-  auto kern = verify_attn_kernel<Tin, D, RG>;
+  const size_t smem = attn_smem_bytes<Tin, D, RG, CPS>(p.S);
+  auto kern = verify_attn_kernel<Tin, D, RG, CPS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
@@ -639,9 +642,10 @@ static cudaError_t launch_attn_t(const AttnParams &p, const CUtensorMap &tmk, co
 
 size_t attn_smem_required(const AttnParams &p) {
   if (p.use_tc) return attn_tc_smem_required(p);
-  if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4>(p.S);
-  if (p.D == 64) return attn_smem_bytes<__nv_bfloat16, 64, 4>(p.S);
-  return attn_smem_bytes<__nv_bfloat16, 128, 4>(p.S);
+  if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4, 1>(p.S);
+  if (p.cps == 2) return p.D == 64 ? attn_smem_bytes<__nv_bfloat16, 64, 2, 2>(p.S) : attn_smem_bytes<__nv_bfloat16, 128, 2, 2>(p.S);
+  if (p.D == 64) return attn_smem_bytes<__nv_bfloat16, 64, 4, 1>(p.S);
+  return attn_smem_bytes<__nv_bfloat16, 128, 4, 1>(p.S);
 }
 
 cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
@@ -652,13 +656,13 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
   } else if (p.dtype == VA_DTYPE_FP32) {
     e = launch_attn_t<float, 64, 4>(p, tmk, tmv, grid, stream);
   } else if (p.D == 64) {
-    e = p.RG == 1 ? launch_attn_t<__nv_bfloat16, 64, 1>(p, tmk, tmv, grid, stream)
-        : p.RG == 2 ? launch_attn_t<__nv_bfloat16, 64, 2>(p, tmk, tmv, grid, stream)
-                    : launch_attn_t<__nv_bfloat16, 64, 4>(p, tmk, tmv, grid, stream);
+    e = p.RG == 1 ? launch_attn_t<__nv_bfloat16, 64, 1, 2>(p, tmk, tmv, grid, stream)
+        : p.RG == 2 ? launch_attn_t<__nv_bfloat16, 64, 2, 2>(p, tmk, tmv, grid, stream)
+                    : launch_attn_t<__nv_bfloat16, 64, 4, 1>(p, tmk, tmv, grid, stream);
   } else {
-    e = p.RG == 1 ? launch_attn_t<__nv_bfloat16, 128, 1>(p, tmk, tmv, grid, stream)
-        : p.RG == 2 ? launch_attn_t<__nv_bfloat16, 128, 2>(p, tmk, tmv, grid, stream)
-                    : launch_attn_t<__nv_bfloat16, 128, 4>(p, tmk, tmv, grid, stream);
+    e = p.RG == 1 ? launch_attn_t<__nv_bfloat16, 128, 1, 2>(p, tmk, tmv, grid, stream)
+        : p.RG == 2 ? launch_attn_t<__nv_bfloat16, 128, 2, 2>(p, tmk, tmv, grid, stream)
+                    : launch_attn_t<__nv_bfloat16, 128, 4, 1>(p, tmk, tmv, grid, stream);
   }
   if (e != cudaSuccess) return e;
 

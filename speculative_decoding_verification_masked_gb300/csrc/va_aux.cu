@@ -51,7 +51,7 @@ cudaError_t launch_tree_mask(int B, int T, const int32_t *parent, uint32_t *mask
 constexpr int kIdxThreads = 1024;
 constexpr int kIdxMaxL = 131072;
 constexpr int kIdxBitmapWords = kIdxMaxL / 32 + 4;
-constexpr int kIdxCacheKeys = 45056;  // keys held in shared memory when L fits
+constexpr int kIdxCacheKeys = 36864;  // keys held in shared memory when L fits
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -125,19 +125,23 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
   int shift = 24;
   bool exact_bucket = false;
   for (; shift >= 0; shift -= 8) {
-    if (tid < 256) sm.hist[tid] = 0;
+    // per-warp private histograms (hist + 256 * warp), then summed per bin
+    for (int j = tid; j < 32 * 256; j += kIdxThreads) sm.hist[j] = 0;
     __syncthreads();
+    uint32_t *myhist = sm.hist + 256 * warp;
     for (int base = 0; base < L; base += kIdxThreads) {
       const int i = base + tid;
-      uint32_t key = 0;
-      bool valid = false;
       if (i < L) {
-        key = key_at(i);
-        valid = key != 0u && (key & pmask) == prefix;
+        const uint32_t key = key_at(i);
+        if (key != 0u && (key & pmask) == prefix) atomicAdd(myhist + ((key >> shift) & 255u), 1u);
       }
-      const uint32_t digit = valid ? (key >> shift) & 255u : 256u + lane;
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (valid && lane == __ffs(peers) - 1) atomicAdd(sm.hist + digit, (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t tot = 0;
+#pragma unroll 8
+      for (int w = 0; w < 32; ++w) tot += sm.hist[256 * w + tid];
+      sm.hist[tid] = tot;  // bin totals in the first 256 entries (warp 0's copy, already read)
     }
     __syncthreads();
     if (warp == 0) {
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   IdxSmem sm;
   sm.bitmap = ism;
   sm.hist = ism + kIdxBitmapWords;
-  sm.scratch = reinterpret_cast<int *>(sm.hist + 256);
+  sm.scratch = reinterpret_cast<int *>(sm.hist + 32 * 256);
   sm.keys = reinterpret_cast<uint32_t *>(sm.scratch + 128);
   const int tid = threadIdx.x;
   const int b = blockIdx.x / p.Hkv;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
 }
 
 size_t build_index_smem_bytes() {
-  return sizeof(uint32_t) * (kIdxBitmapWords + 256 + 128 + kIdxCacheKeys);
+  return sizeof(uint32_t) * (kIdxBitmapWords + 32 * 256 + 128 + kIdxCacheKeys);
 }
 
 cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,

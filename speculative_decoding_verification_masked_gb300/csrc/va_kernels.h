@@ -19,6 +19,7 @@ struct AttnParams {
   int S;       // segments = B * Hkv * NRB
   int rows_pad;// rows per segment slot in the partial buffers
   int use_tc;  // 1: tcgen05 kernel (bf16, D 128, more than 64 packed rows)
+  int cps;     // CTAs of the attention kernel resident per SM (1 or 2)
   float scale;
   va_dtype dtype;
   int layout;  // va_layout
