@@ -321,6 +321,22 @@ def load_peak_hbm():
 # main
 # ----------------------------------------------------------------------------
 
+def run_profile(args):
+    """A fixed number of eager verification steps of one workload: the
+    command the committed ncu summaries are taken from."""
+    import speculative_decoding_verification_masked_gb300 as va
+
+    torch.cuda.set_device(0)
+    va.api.lib(build_if_missing=False)
+    case = DeviceCase(W.make_workload(args.profile, seed=0), va)
+    for _ in range(args.calls):
+        case.step()
+    torch.cuda.synchronize()
+    va.verify_attn_check_status(case.ws)
+    print(json.dumps({"profile": args.profile, "calls": args.calls, "status": "ok"}))
+    return 0
+
+
 def dist_setup(n):
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
@@ -435,11 +451,16 @@ def main():
     ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES), default=None,
+                    help="run --calls plain verification steps of one workload (for ncu) and exit")
+    ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile is not None:
+        return run_profile(args)
 
     rank, world, local, dist = dist_setup(args.gpus)
     import speculative_decoding_verification_masked_gb300 as va

@@ -6,7 +6,7 @@
 // 64-key tiles), but every K/V tile read from HBM now feeds up to 256 query
 // rows through UMMA instead of warp-level mma.sync.
 //
-// Roles (10 warps when the segment has two 128-row M-tiles):
+// Roles (11 warps when the segment has two 128-row M-tiles):
 //   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
 //                    = one TMEM lane.  Reads S from TMEM, applies the draft
 //                    bitmask, runs the online softmax, writes P (bf16) back
@@ -14,10 +14,13 @@
 //                    more than 2^8, and writes the output row.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
 //                    sparse) into a 4-stage ring (shared with the other kernel)
-//   warp 4*NMT+1     MMA issuer: S_i = Q_i K^T (M128 N64 K128, both operands in
-//                    shared memory, K-major 128B swizzle) into a double-buffered
-//                    TMEM slot, and O_i += P_i V (A = P from TMEM, B = V as an
-//                    MN-major operand); owns the TMEM allocation.
+//   warps 4*NMT+1+i  MMA issuer of M-tile i: S_i = Q_i K^T (M128 N64 K128, both
+//                    operands in shared memory, K-major 128B swizzle) into a
+//                    double-buffered TMEM slot, and O_i += P_i V (A = P from
+//                    TMEM, B = V as an MN-major operand).  A chain of dependent
+//                    MMAs issues at MMA latency, so one issuer per M-tile keeps
+//                    two independent chains in the tensor pipe.  Issuer 0 owns
+//                    the TMEM allocation.
 // TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
 // Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
 // barrier sequence of all roles intact, drains and frees TMEM.
@@ -121,7 +124,7 @@ struct TcSmem {
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kTstartOff = kMiscOff + 16;
-  static constexpr int kThreads = (4 * NMT + 2) * 32;
+  static constexpr int kThreads = (5 * NMT + 1) * 32;
 };
 
 // Offset of chunk c (16 B) of row r in a 128-row, 128B-swizzled Q tile pair.
@@ -139,7 +142,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   constexpr int NS = kTcStages;
   constexpr int kSoftThreads = 128 * NMT;
   constexpr int kProducerWarp = 4 * NMT;
-  constexpr int kMmaWarp = 4 * NMT + 1;
+  constexpr int kMmaWarp0 = 4 * NMT + 1;  // issuer of M-tile i is warp kMmaWarp0 + i
+  constexpr int kMmaThreads = 32 * NMT;
   constexpr int kBarQ = 1, kBarSoft = 2, kBarEnd = 3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, use_tma ? 1 : 32);
-      mbar_init(empty + i, 1);
+      mbar_init(empty + i, NMT);  // one arrive per M-tile issuer
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(s_full + i, 1);
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     }
     mbar_init(o_done + 0, 1);
     mbar_init(o_done + 1, 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, NMT);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -190,20 +194,21 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   }
 
   // TMEM: 512 columns, allocated by the MMA warp
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  named_bar_sync(kBarEnd, kSoftThreads + 32);
+  named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const float cl2 = p.scale * kLog2e;
   const int group = p.Hq / p.Hkv;
 
-  if (warp == kMmaWarp) {
-    // ================================ MMA issuer ================================
+  if (warp >= kMmaWarp0) {
+    // =========================== MMA issuer of M-tile mi ===========================
+    const int mi = warp - kMmaWarp0;
     const uint32_t id_s = umma_idesc(128, 64, 0);
     const uint32_t id_o = umma_idesc(128, 128, 1);
     int it = 0, jt = 0;
@@ -263,38 +268,33 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const Seg g = seg_info(p, s, false);
       const int lt0 = max(tstart[s], t0) - tstart[s];
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
-      named_bar_sync(kBarQ, kSoftThreads + 32);  // Q of this segment is in shared memory
+      named_bar_sync(kBarQ, kSoftThreads + kMmaThreads);  // Q of this segment is in shared memory
       acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
-      for (int i = 0; i < NMT; ++i) issue_s(i, jt & 1, it % NS);
+      issue_s(mi, jt & 1, it % NS);
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int st = it % NS;
         const int b = jt & 1;
-        const uint32_t pph = (uint32_t)(jt >> 1) & 1u;
-        const bool has_next = lt + 1 < lt1;
         const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
-        // M-tiles in turn: PV_i(lt), then -- once it has completed -- S_i(lt+1), so
-        // each warpgroup's softmax overlaps the other M-tile's MMAs and no MMA of
-        // an M-tile runs while that M-tile's softmax reads or writes TMEM
-        for (int i = 0; i < NMT; ++i) {
-          wait_ok(p_full + 2 * i + b, pph);
-          issue_pv(i, b, st, lt == lt0, exact);
-          wait_ok(o_done + i, (uint32_t)jt & 1u);
-          tc_fence_after();
-          if (i == NMT - 1 && lane == 0) mbar_arrive(empty + st);  // every PV of this tile is done
-          if (has_next) {
-            if (i == 0) acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
-            issue_s(i, b ^ 1, (it + 1) % NS);
-          }
+        // PV(lt), then -- once it has completed -- S(lt+1) into the other buffer:
+        // no MMA of this M-tile runs while its softmax reads or writes TMEM
+        wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+        issue_pv(mi, b, st, lt == lt0, exact);
+        wait_ok(o_done + mi, (uint32_t)jt & 1u);
+        tc_fence_after();
+        if (lane == 0) mbar_arrive(empty + st);  // this M-tile is done with the K/V stage
+        if (lt + 1 < lt1) {
+          acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
+          issue_s(mi, b ^ 1, (it + 1) % NS);
         }
       }
     }
-    // drain: every MMA this warp issued has finished before TMEM is released
+    // drain: every MMA the issuers started has finished before TMEM is released
     if (lane == 0) umma_commit(drain);
     mbar_wait(drain, 0u, p.wait_ns);
     tc_fence_before();
-    named_bar_sync(kBarEnd, kSoftThreads + 32);
+    named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    if (mi == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     return;
   }
 
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       }
       fence_proxy_async_smem();
     }
-    named_bar_arrive(kBarQ, kSoftThreads + 32);
+    named_bar_arrive(kBarQ, kSoftThreads + kMmaThreads);
 
     const int rr = g.rb * p.rows_pad + mi * 128 + r;
     const bool rvalid = rr < p.R;
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     }
   }
   tc_fence_before();
-  named_bar_sync(kBarEnd, kSoftThreads + 32);
+  named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);
 }
 
 // ---------------------------------------------------------------------------
