@@ -184,7 +184,8 @@ va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k
  * normalised over its own keys), lse_parts [n_parts][n_rows] fp32 natural
  * log (-inf = empty part) -> out [n_rows][D] of out_dtype, lse [n_rows] fp32
  * (lse may be NULL).  Exposed for merging parts computed elsewhere, e.g. by
- * other ranks of a context-parallel split.  D in {64, 128}, n_parts <= 1024.
+ * other ranks of a context-parallel split.  D in {64, 128}, n_parts <= 1024,
+ * o_parts 16-byte aligned (VA_ERR_INVALID_ARG otherwise).
  */
 va_status verify_attn_combine(int n_rows, int n_parts, int D, const float *o_parts,
                               const float *lse_parts, va_dtype out_dtype, void *out, float *lse,

@@ -346,6 +346,7 @@ va_status verify_attn_combine(int n_rows, int n_parts, int D, const float *o_par
   if (out_dtype != VA_DTYPE_BF16 && out_dtype != VA_DTYPE_FP32) return fail(VA_ERR_INVALID_ARG, "unknown out dtype");
   if (o_parts == nullptr || lse_parts == nullptr || out == nullptr)
     return fail(VA_ERR_INVALID_ARG, "o_parts, lse_parts and out must not be NULL");
+  if (!aligned(o_parts, 16)) return fail(VA_ERR_INVALID_ARG, "o_parts must be 16-byte aligned");
   if (n_rows == 0) return ok();
   cudaError_t e =
       va::launch_combine_generic(n_rows, n_parts, D, o_parts, lse_parts, out_dtype, out, lse, (cudaStream_t)stream);

@@ -515,108 +515,126 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16 *dst, flo
   *dst = __float2bfloat16_rn(v);
 }
 
-// Merge the parts of the rows handled by one block (blockDim = 128 threads,
-// 128 / D rows).  Part weights are computed once per row into shared memory
-// (every part's lse is read by one thread), then each thread accumulates its
-// d-column over the parts with eight loads in flight.
+// Merge the parts of one row with a block of 128 threads.  Thread (g, c) holds
+// the four columns [4c, 4c + 4) of the parts s = g (mod PG), PG = 128 / (D / 4),
+// in registers; the first batch of those loads is issued together with the
+// loads of the parts' lse, so a merge of up to PG * kCombineBatch parts costs
+// one round trip to L2.  The part weights e^(lse_s - M) go to shared memory.
 constexpr int kMaxCombineParts = 1024;
+constexpr int kCombineBatch = 16;
 
 template <typename OutT>
-__device__ __forceinline__ void combine_rows(int n_parts, int D, const float *o, size_t o_stride, const float *l,
-                                             size_t l_stride, OutT *out, float *lse_out, float *wsm, bool active) {
-  const int rows = blockDim.x / D;
-  const int ri = threadIdx.x / D;  // row of this thread within the block
-  const int d = threadIdx.x % D;
-  float *w = wsm + ri * kMaxCombineParts;
-  __shared__ float red[8];
-  // 1) lse of every part -> shared memory, row max
+__device__ __forceinline__ void combine_row(int n_parts, int D, const float *o, size_t o_stride, const float *l,
+                                            size_t l_stride, OutT *out, float *lse_out) {
+  __shared__ float w[kMaxCombineParts];
+  __shared__ float red_m[4], red_s[4];
+  __shared__ float4 accs[128];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = D >> 2;     // float4 columns of a row
+  const int PG = 128 / q;   // part groups
+  const int c = tid % q, g = tid / q;
   float mloc = -INFINITY;
-  for (int s = d; s < n_parts; s += D) {
-    const float ls = active ? l[s * l_stride] : -INFINITY;
+  for (int s = tid; s < n_parts; s += 128) {
+    const float ls = __ldg(l + (size_t)s * l_stride);
     w[s] = ls;
     mloc = fmaxf(mloc, ls);
   }
+  float4 v[kCombineBatch];
+#pragma unroll
+  for (int j = 0; j < kCombineBatch; ++j) {
+    const int s = g + j * PG;
+    v[j] = s < n_parts ? __ldg(reinterpret_cast<const float4 *>(o + (size_t)s * o_stride) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  const int wib = d >> 5;  // warp within the row
-  const int nw = D >> 5;
-  if ((threadIdx.x & 31) == 0) red[ri * nw + wib] = mloc;
+  if (lane == 0) red_m[warp] = mloc;
   __syncthreads();
-  float M = -INFINITY;
-  for (int i = 0; i < nw; ++i) M = fmaxf(M, red[ri * nw + i]);
-  __syncthreads();
-  // 2) weights e^(lse_s - M) and their sum
+  const float M = fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3]));
   float sloc = 0.f;
-  for (int s = d; s < n_parts; s += D) {
+  for (int s = tid; s < n_parts; s += 128) {
     const float ls = w[s];
     const float e = (M == -INFINITY || ls == -INFINITY) ? 0.f : __expf(ls - M);
     w[s] = e;
     sloc += e;
   }
   for (int off = 16; off > 0; off >>= 1) sloc += __shfl_xor_sync(0xffffffffu, sloc, off);
-  if ((threadIdx.x & 31) == 0) red[ri * nw + wib] = sloc;
+  if (lane == 0) red_s[warp] = sloc;
   __syncthreads();
-  float Lsum = 0.f;
-  for (int i = 0; i < nw; ++i) Lsum += red[ri * nw + i];
-  (void)rows;
-  // 3) out = sum_s w_s o_s / sum_s w_s
-  float acc = 0.f;
-  if (active) {
-    int s = 0;
-    for (; s + 8 <= n_parts; s += 8) {
-      float v[8];
+  const float Lsum = (red_s[0] + red_s[1]) + (red_s[2] + red_s[3]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = o[(size_t)(s + u) * o_stride + d];
+  for (int j = 0; j < kCombineBatch; ++j) {
+    const int s = g + j * PG;
+    const float ws = s < n_parts ? w[s] : 0.f;
+    acc.x = fmaf(ws, v[j].x, acc.x);
+    acc.y = fmaf(ws, v[j].y, acc.y);
+    acc.z = fmaf(ws, v[j].z, acc.z);
+    acc.w = fmaf(ws, v[j].w, acc.w);
+  }
+  for (int base = PG * kCombineBatch; base < n_parts; base += PG * kCombineBatch) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc = fmaf(w[s + u], v[u], acc);
+    for (int j = 0; j < kCombineBatch; ++j) {
+      const int s = base + g + j * PG;
+      v[j] = s < n_parts ? __ldg(reinterpret_cast<const float4 *>(o + (size_t)s * o_stride) + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (; s < n_parts; ++s) acc = fmaf(w[s], o[(size_t)s * o_stride + d], acc);
-    const float r = Lsum > 0.f ? acc / Lsum : 0.f;
-    store_out<OutT>(out + d, r);
-    if (d == 0 && lse_out != nullptr) *lse_out = Lsum > 0.f ? M + __logf(Lsum) : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) {
+      const int s = base + g + j * PG;
+      const float ws = s < n_parts ? w[s] : 0.f;
+      acc.x = fmaf(ws, v[j].x, acc.x);
+      acc.y = fmaf(ws, v[j].y, acc.y);
+      acc.z = fmaf(ws, v[j].z, acc.z);
+      acc.w = fmaf(ws, v[j].w, acc.w);
+    }
+  }
+  accs[tid] = acc;
+  __syncthreads();
+  if (tid < D) {
+    const int cc = tid >> 2, k = tid & 3;
+    float r = 0.f;
+    for (int gg = 0; gg < PG; ++gg) {
+      const float4 a = accs[gg * q + cc];
+      r += k == 0 ? a.x : k == 1 ? a.y : k == 2 ? a.z : a.w;
+    }
+    store_out<OutT>(out + tid, Lsum > 0.f ? r / Lsum : 0.f);
+    if (tid == 0 && lse_out != nullptr) *lse_out = Lsum > 0.f ? M + __logf(Lsum) : -INFINITY;
   }
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(128) combine_segments_kernel(const AttnParams p, int rpb_shift) {
-  __shared__ float wsm[2 * kMaxCombineParts];
+__global__ void __launch_bounds__(128) combine_segments_kernel(const AttnParams p) {
   // wait until every CTA of the attention grid has finished and flushed
   pdl_wait_primary();
   const int D = p.D;
-  const int rows_per_block = 1 << rpb_shift;
-  const int row_g = blockIdx.x * rows_per_block + (threadIdx.x / D);
-  const int s = row_g / p.rows_pad;
-  const int row = row_g % p.rows_pad;
-  // rows of one block share a segment (rows_pad is a multiple of the rows per block)
-  const int sb = (blockIdx.x * rows_per_block) / p.rows_pad;
-  if (sb >= p.S) return;
-  const int2 meta = p.meta[sb];
+  const int s = blockIdx.x / p.rows_pad;
+  const int row = blockIdx.x % p.rows_pad;
+  if (s >= p.S) return;
+  const int2 meta = p.meta[s];
   if (meta.y <= 1) return;
   const int rb = s % p.NRB;
   const int hkv = (s / p.NRB) % p.Hkv;
   const int b = s / (p.NRB * p.Hkv);
   const int rr = rb * p.rows_pad + row;
-  const bool active = rr < p.R;
+  if (rr >= p.R) return;
   const int group = p.Hq / p.Hkv;
-  const int t = active ? rr / group : 0;
-  const int hq = hkv * group + (active ? rr % group : 0);
+  const int t = rr / group;
+  const int hq = hkv * group + rr % group;
   const size_t slot0 = (size_t)meta.x;
   const float *o = p.o_part + (slot0 * p.rows_pad + row) * D;
   const float *l = p.lse_part + slot0 * p.rows_pad + row;
   OutT *out = static_cast<OutT *>(p.out) + (((size_t)b * p.T + t) * p.Hq + hq) * D;
   float *lse = p.lse + ((size_t)b * p.Hq + hq) * p.T + t;
-  combine_rows<OutT>(meta.y, D, o, (size_t)p.rows_pad * D, l, (size_t)p.rows_pad, out, lse, wsm, active);
+  combine_row<OutT>(meta.y, D, o, (size_t)p.rows_pad * D, l, (size_t)p.rows_pad, out, lse);
 }
 
 template <typename OutT>
 __global__ void __launch_bounds__(128) combine_generic_kernel(int n_rows, int n_parts, int D, const float *o_parts,
                                                               const float *lse_parts, OutT *out, float *lse) {
-  __shared__ float wsm[2 * kMaxCombineParts];
-  const int rows_per_block = 128 / D;
-  const int r = blockIdx.x * rows_per_block + threadIdx.x / D;
-  const bool active = r < n_rows;
-  const int rc = active ? r : 0;
-  combine_rows<OutT>(n_parts, D, o_parts + (size_t)rc * D, (size_t)n_rows * D, lse_parts + rc, (size_t)n_rows,
-                     out + (size_t)rc * D, lse != nullptr ? lse + rc : nullptr, wsm, active);
+  const int r = blockIdx.x;
+  if (r >= n_rows) return;
+  combine_row<OutT>(n_parts, D, o_parts + (size_t)r * D, (size_t)n_rows * D, lse_parts + r, (size_t)n_rows,
+                    out + (size_t)r * D, lse != nullptr ? lse + r : nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -667,10 +685,9 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
   if (e != cudaSuccess) return e;
 
   // combine, chained by programmatic dependent launch
-  const int rpb_shift = p.D == 64 ? 1 : 0;
   const long long rows = (long long)p.S * p.rows_pad;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((rows + (1 << rpb_shift) - 1) >> rpb_shift));
+  cfg.gridDim = dim3((unsigned)rows);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -680,16 +697,15 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.dtype == VA_DTYPE_FP32)
-    e = cudaLaunchKernelEx(&cfg, combine_segments_kernel<float>, p, rpb_shift);
+    e = cudaLaunchKernelEx(&cfg, combine_segments_kernel<float>, p);
   else
-    e = cudaLaunchKernelEx(&cfg, combine_segments_kernel<__nv_bfloat16>, p, rpb_shift);
+    e = cudaLaunchKernelEx(&cfg, combine_segments_kernel<__nv_bfloat16>, p);
   return e;
 }
 
 cudaError_t launch_combine_generic(int n_rows, int n_parts, int D, const float *o_parts, const float *lse_parts,
                                    va_dtype out_dtype, void *out, float *lse, cudaStream_t stream) {
-  const int rpb = 128 / D;
-  const dim3 grid((unsigned)((n_rows + rpb - 1) / rpb));
+  const dim3 grid((unsigned)n_rows);
   if (out_dtype == VA_DTYPE_FP32)
     combine_generic_kernel<float><<<grid, 128, 0, stream>>>(n_rows, n_parts, D, o_parts, lse_parts,
                                                             static_cast<float *>(out), lse);
