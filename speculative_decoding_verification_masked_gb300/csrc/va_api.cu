@@ -111,6 +111,13 @@ struct RowPlan {
 // Kernel choice and row blocking.  More than 64 packed rows (bf16, D 128) go to
 // the tcgen05 kernel in blocks of up to 256 rows (two 128-row M-tiles); the
 // rest to the mma.sync kernel in blocks of 16, 32 or 64 rows.
+// The keys-on-lanes tcgen05 kernel serves bf16 d128 segments of at most 64
+// rows; VA_SMALL_ROWS_KERNEL=mma selects the mma.sync kernel for them instead.
+bool tck_enabled() {
+  const char *e = getenv("VA_SMALL_ROWS_KERNEL");
+  return !(e != nullptr && strcmp(e, "mma") == 0);
+}
+
 RowPlan row_plan(const va_shape &s) {
   RowPlan r;
   r.R = (s.Hq / s.Hkv) * s.T;
@@ -122,6 +129,10 @@ RowPlan row_plan(const va_shape &s) {
     r.use_tc = 1;
     r.RG = 4;
     r.rows_pad = r.R > 128 ? 256 : 128;
+  } else if (s.D == 128 && tck_enabled()) {
+    r.use_tc = 2;
+    r.RG = 4;
+    r.rows_pad = r.R <= 16 ? 16 : (r.R <= 32 ? 32 : 64);
   } else {
     r.RG = r.R <= 16 ? 1 : (r.R <= 32 ? 2 : 4);
     r.rows_pad = 16 * r.RG;
@@ -232,6 +243,7 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.mask = c.mask;
   p.mask_words = (s.T + 31) / 32;
   p.out = c.out;
+  p.out_align16 = aligned(c.out, 16) ? 1 : 0;
   p.lse = c.lse;
   const va::WsLayout wl = va::ws_layout(rp.S, rp.S + rp.cps * sms, rp.rows_pad, s.D);
   uint8_t *ws = static_cast<uint8_t *>(c.ws);
@@ -243,7 +255,8 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
 
   // key tiles an upper bound can produce; the grid never exceeds them
   long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
-  const long long tiles_cap = (long long)rp.S * ((keys_cap + 63) / 64);
+  const long long tile_keys = rp.use_tc == 2 ? 128 : 64;
+  const long long tiles_cap = (long long)rp.S * ((keys_cap + tile_keys - 1) / tile_keys);
   if (tiles_cap >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "problem too large (%lld key tiles)", tiles_cap);
   const long long ctas = (long long)rp.cps * sms;
   const int grid = (int)(tiles_cap < ctas ? tiles_cap : ctas);

@@ -659,7 +659,8 @@ static cudaError_t launch_attn_t(const AttnParams &p, const CUtensorMap &tmk, co
 }
 
 size_t attn_smem_required(const AttnParams &p) {
-  if (p.use_tc) return attn_tc_smem_required(p);
+  if (p.use_tc == 1) return attn_tc_smem_required(p);
+  if (p.use_tc == 2) return attn_tck_smem_required(p);
   if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4, 1>(p.S);
   if (p.cps == 2) return p.D == 64 ? attn_smem_bytes<__nv_bfloat16, 64, 2, 2>(p.S) : attn_smem_bytes<__nv_bfloat16, 128, 2, 2>(p.S);
   if (p.D == 64) return attn_smem_bytes<__nv_bfloat16, 64, 4, 1>(p.S);
@@ -669,8 +670,10 @@ size_t attn_smem_required(const AttnParams &p) {
 cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                              cudaStream_t stream) {
   cudaError_t e;
-  if (p.use_tc) {
+  if (p.use_tc == 1) {
     e = launch_attention_tc(p, tmk, tmv, grid, stream);
+  } else if (p.use_tc == 2) {
+    e = launch_attention_tck(p, tmk, tmv, grid, stream);
   } else if (p.dtype == VA_DTYPE_FP32) {
     e = launch_attn_t<float, 64, 4>(p, tmk, tmv, grid, stream);
   } else if (p.D == 64) {

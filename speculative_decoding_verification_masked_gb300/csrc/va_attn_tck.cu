@@ -1,0 +1,662 @@
+// Verification attention on the 5th-generation tensor cores with the KEYS on
+// the TMEM lanes, for segments of at most 64 packed query rows (GQA group x T
+// draft tokens; a chain of 8 drafts with group 4 gives 32 rows).  One MMA has
+// M = 128, so rather than padding 32 query rows to 128 the products are taken
+// transposed, with a 128-key tile as the M side:
+//
+//   S^T (128 keys x NR rows)   = K (128 x d) . Q^T       A = K tile, K-major; B = Q, K-major
+//   O^T (128 d x NR rows)     += V^T . P^T               A = V tile, MN-major; B = P^T, MN-major
+//   l   (NR rows, every lane) += 1 (128 x 128) . P^T     A = ones held in TMEM
+//
+// (LongSpec 2.C: the unmasked prefix and the masked draft block are the same
+// tile loop, the draft block being the last tiles of a segment; partial
+// results of a segment split over CTAs are merged by the exact log-sum-exp
+// combine.)  The row sums l come from the tensor core too, so the normaliser
+// uses exactly the bf16 P that the numerator used.
+//
+// Roles (6 warps, one CTA per SM):
+//   warps 0-3  softmax: thread k owns key k of the tile (TMEM lane k) and all
+//              NR rows of it.  Scores are taken in log2 units against a
+//              per-row reference max that moves only when some score of the
+//              tile exceeds it by more than 2^8 (exact either way: the
+//              exponentials stay below 2^8 and O, l are rescaled when it
+//              moves); whether it must move is one block-wide vote (bar.red),
+//              and only then are the row maxima reduced across the 128 keys.
+//              P (bf16; on draft tiles also the bf16 residual) is written as
+//              the MN-major P^T operand over the K tile of the same stage,
+//              which the S MMA has finished reading.  In the epilogue thread
+//              d owns output column d.
+//   warp 4     producer: TMA boxes (dense) or cp.async gathers (paged, sparse)
+//              into a 3-stage ring of 128-key K and V tiles (64 KB a stage)
+//   warp 5     MMA issuer and TMEM owner: S of tile i+2 is issued as soon as
+//              the softmax of tile i has released its S buffer.
+// TMEM columns (NC = max(NR, 32)): O^T at 0, l at NC, S buffers at 2NC and
+// 3NC, the ones operand at 4NC.  Every wait is bounded; on timeout the CTA
+// records VA_ERR_TIMEOUT, keeps the barrier sequence of all roles, drains and
+// frees TMEM.
+#include <cuda.h>
+#include <math.h>
+
+#include "va_common.cuh"
+#include "va_kernels.h"
+#include "va_pipeline.cuh"
+#include "va_tcgen05.cuh"
+
+namespace va {
+
+constexpr int kTkKeys = 128;  // keys per tile
+constexpr int kTkStages = 3;
+constexpr int kTkThreads = 192;
+
+template <int NR>
+struct TkSmem {
+  using Geo = StageGeom<__nv_bfloat16, 128, kTkKeys>;
+  static constexpr int kStageBytes = Geo::kStageBytes;  // 64 KB
+  static constexpr int kQOff = kTkStages * kStageBytes;
+  static constexpr int kQBytes = 2 * NR * 128;  // two 128-byte columns of NR rows
+  static constexpr int kBarOff = kQOff + kQBytes;
+  // barriers: full[3], empty[3], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 2 * kTkStages + 7;
+  static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // tmem base, abort flag
+  static constexpr int kRowMaskOff = kMiscOff + 16;        // u64 [64]: draft visibility rows
+  static constexpr int kKeyMaskOff = kRowMaskOff + 512;    // u64 [64]: per draft key, rows that see it
+  static constexpr int kRedOff = kKeyMaskOff + 512;        // float4 [NR]: per-warp row maxima
+  static constexpr int kRowInvOff = kRedOff + NR * 16;     // float [64]: 1 / l per row (epilogue)
+  static constexpr int kTstartOff = kRowInvOff + 256;
+  static_assert(kQOff % 1024 == 0 && kQBytes % 1024 == 0, "UMMA operands need 1024-byte aligned swizzle atoms");
+  static_assert(kBarOff % 8 == 0 && kRowMaskOff % 8 == 0 && kKeyMaskOff % 8 == 0, "8-byte alignment");
+  static_assert(kRedOff % 16 == 0, "float4 array needs 16-byte alignment");
+  static_assert(kRowInvOff % 16 == 0, "vector loads of the row constants");
+  static constexpr int kNC = NR < 32 ? 32 : NR;            // TMEM columns per region
+  static constexpr int kTmemCols = NR <= 32 ? 256 : 512;
+};
+
+// Row-wise block of a warp: v[N] per lane -> lane holds the warp maximum of
+// max(N/32, 1) rows (row j + (N/32)*lane for N >= 32, lane / (32/N) below).
+template <int N, int O>
+struct WarpScatterMax {
+  static __device__ __forceinline__ void run(float *v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (N >= 2) {
+      constexpr int H = N / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+      }
+      WarpScatterMax<H, O / 2>::run(v, lane);
+    } else {
+      v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
+      WarpScatterMax<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+// Block-wide OR of a predicate over the `n` threads of named barrier `id`
+// (also a barrier for them).
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// NR fp32 columns of this thread's TMEM lane.
+template <int NR>
+__device__ __forceinline__ void tmem_ld_f(uint32_t taddr, float (&x)[NR]) {
+  if constexpr (NR == 8) {
+    uint32_t u[8];
+    tmem_ld8(taddr, u);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(u[j]);
+  } else if constexpr (NR == 16) {
+    uint32_t u[16];
+    tmem_ld16(taddr, u);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(u[j]);
+  } else {
+#pragma unroll
+    for (int h = 0; h < NR / 32; ++h) {
+      uint32_t u[32];
+      tmem_ld32(taddr + 32 * h, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[32 * h + j] = __uint_as_float(u[j]);
+    }
+  }
+}
+
+// Multiply column j of this lane's NR columns at taddr by a[j].
+template <int NR>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float *a) {
+  if constexpr (NR == 16) {
+    uint32_t u[16];
+    tmem_ld16(taddr, u);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * a[j]);
+    tmem_st16(taddr, u);
+  } else {
+#pragma unroll
+    for (int h = 0; h < NR / 32; ++h) {
+      uint32_t u[32];
+      tmem_ld32(taddr + 32 * h, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * a[32 * h + j]);
+      tmem_st32(taddr + 32 * h, u);
+    }
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kTkThreads, 1)
+    verify_attn_tck_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                           const __grid_constant__ CUtensorMap tmv) {
+  using SM = TkSmem<NR>;
+  using Geo = typename SM::Geo;
+  constexpr int D = 128;
+  constexpr int TK = kTkKeys;
+  constexpr int NS = kTkStages;
+  constexpr int NC = SM::kNC;
+  constexpr int kSoft = 128;
+  constexpr int kProducerWarp = 4, kMmaWarp = 5;
+  constexpr int kBarQ = 1, kBarRed = 2, kBarSoft = 3, kBarEnd = 4;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t *stages = smem;
+  uint8_t *sQ = smem + SM::kQOff;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBarOff);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + NS;
+  uint64_t *s_full = bars + 2 * NS;      // [b]
+  uint64_t *p_full = bars + 2 * NS + 2;  // [b]
+  uint64_t *o_done = bars + 2 * NS + 4;  // [tile & 1]
+  uint64_t *drain = bars + 2 * NS + 6;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
+  uint64_t *rowmask = reinterpret_cast<uint64_t *>(smem + SM::kRowMaskOff);
+  uint64_t *keymask = reinterpret_cast<uint64_t *>(smem + SM::kKeyMaskOff);
+  float4 *red = reinterpret_cast<float4 *>(smem + SM::kRedOff);
+  float *row_inv = reinterpret_cast<float *>(smem + SM::kRowInvOff);
+  int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  const bool use_tma = p.layout == VA_LAYOUT_DENSE;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = blockIdx.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, use_tma ? 1 : 32);
+      mbar_init(empty + i, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, kSoft);
+    }
+    mbar_init(o_done + 0, 1);
+    mbar_init(o_done + 1, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const CtaRange cr = plan_cta<TK>(p, tstart);  // contains __syncthreads
+  if (c >= cr.G) {
+    pdl_launch_dependents();
+    return;
+  }
+  const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
+
+  if (warp == kProducerWarp) {
+    bool pok = true;
+    produce_tiles<__nv_bfloat16, D, NS, TK, 2>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag,
+                                               use_tma, pok);
+    pdl_launch_dependents();
+    return;
+  }
+
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(SM::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  named_bar_sync(kBarEnd, kSoft + 32);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const float cl2 = p.scale * kLog2e;
+  const int group = p.Hq / p.Hkv;
+
+  bool ok = true;
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
+    if (ok && *abort_flag) ok = false;
+    if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
+      record_status(p.status, VA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      ok = false;
+    }
+  };
+
+  if (warp == kMmaWarp) {
+    // ================================ MMA issuer ================================
+    const uint32_t id_s = umma_idesc(128, NR, 0, 0);
+    const uint32_t id_o = umma_idesc(128, NR, 1, 1);
+    const uint32_t id_l = umma_idesc(128, NR, 0, 1);
+    const uint32_t tO = tmem, tL = tmem + NC, tOnes = tmem + 4 * NC;
+    int it = 0, jt = 0;
+    // Shared-memory descriptors are built once; a K-step or stage offset is an
+    // add to the start-address field (addresses stay below 256 KB, so the
+    // 14-bit field never carries).
+    const uint64_t dK0 = umma_sdesc(smem_u32(stages), 16, 1024);                      // K tile, K-major
+    const uint64_t dQ0 = umma_sdesc(smem_u32(sQ), 16, 1024);                          // Q, K-major
+    const uint64_t dV0 = umma_sdesc(smem_u32(stages) + Geo::kTileBytes, TK * 128, 1024);  // V tile, MN-major
+    const uint64_t dP0 = umma_sdesc(smem_u32(stages), 8192, 1024);                    // P^T over the K tile
+    constexpr uint64_t kStageStep = SM::kStageBytes >> 4;
+    auto issue_s = [&](int b, int st) {  // S^T(b) = K Q^T
+      if (!ok || lane != 0) return;
+      tc_fence_after();
+      const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
+      const uint32_t dS = tmem + (2 + b) * NC;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t koff = (uint64_t)(((ks >> 2) * (TK * 128) + (ks & 3) * 32) >> 4);
+        const uint64_t qoff = (uint64_t)(((ks >> 2) * (NR * 128) + (ks & 3) * 32) >> 4);
+        umma_ss(dS, dK + koff, dQ0 + qoff, id_s, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(s_full + b);
+    };
+    auto issue_pv = [&](int st, int b, bool first, bool exact) {  // O^T += V^T P^T, l += 1 P^T
+      if (!ok || lane != 0) return;
+      tc_fence_after();
+      const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
+      const uint64_t dP = dP0 + (uint64_t)st * kStageStep;
+      const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+      for (int kk = 0; kk < TK / 16; ++kk) {
+        const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+        const uint32_t acc = kk > 0 ? 1u : acc0;
+        umma_ss(tO, dV + off, dP + off, id_o, acc);
+        umma_ts(tL, tOnes, dP + off, id_l, acc);
+      }
+      if (exact) {  // the bf16 residual of P on draft tiles
+        constexpr uint64_t lo = (uint64_t)((TK * 128) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < TK / 16; ++kk) {
+          const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+          umma_ss(tO, dV + off, dP + lo + off, id_o, 1u);
+          umma_ts(tL, tOnes, dP + lo + off, id_l, 1u);
+        }
+      }
+      umma_commit(o_done + b);
+      umma_commit(empty + st);  // the stage is free once these MMAs have read it
+    };
+
+    for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
+      const Seg g = seg_info(p, s, false);
+      const int lt0 = max(tstart[s], t0) - tstart[s];
+      const int lt1 = min(tstart[s + 1], t1) - tstart[s];
+      named_bar_sync(kBarQ, kSoft + 32);  // Q of this segment is in shared memory
+      wait_ok(full + it % NS, (uint32_t)(it / NS) & 1u);
+      issue_s(jt & 1, it % NS);
+      if (lt0 + 1 < lt1) {
+        wait_ok(full + (it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u);
+        issue_s((jt + 1) & 1, (it + 1) % NS);
+      }
+      for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
+        const int b = jt & 1;
+        const bool exact = lt * TK + TK > g.n_prefix;  // tile holds draft keys
+        wait_ok(p_full + b, (uint32_t)(jt >> 1) & 1u);
+        issue_pv(it % NS, b, lt == lt0, exact);
+        if (lt + 2 < lt1) {
+          wait_ok(full + (it + 2) % NS, (uint32_t)((it + 2) / NS) & 1u);
+          issue_s(b, (it + 2) % NS);
+        }
+        __syncwarp();
+      }
+    }
+    // drain: every MMA issued has finished before TMEM is released
+    if (lane == 0) umma_commit(drain);
+    mbar_wait(drain, 0u, p.wait_ns);
+    tc_fence_before();
+    named_bar_sync(kBarEnd, kSoft + 32);
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(SM::kTmemCols)
+                 : "memory");
+    pdl_launch_dependents();
+    return;
+  }
+
+  // ================================== softmax ==================================
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tO = tmem + lane_base, tL = tO + NC;
+  {  // the all-ones A operand of the row-sum MMA: 8 columns of bf16 pairs (1.0, 1.0)
+    uint32_t ones[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ones[j] = 0x3F803F80u;
+    tmem_st8(tO + 4 * NC, ones);
+    tmem_st_wait();
+  }
+  int it = 0, jt = 0;
+  for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
+    const Seg g = seg_info(p, s, false);
+    const int lt0 = max(tstart[s], t0) - tstart[s];
+    const int lt1 = min(tstart[s + 1], t1) - tstart[s];
+    const int first_cta = owner_cta(tstart[s], cr.total, cr.G);
+    const int n_parts = owner_cta(tstart[s + 1] - 1, cr.total, cr.G) - first_cta + 1;
+    if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
+
+    // ---- Q of this segment into shared memory: [2 columns][NR rows][128 B], 128B swizzle ----
+    // (the previous segment's MMAs have completed: its epilogue waited for the last one)
+    {
+      const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+      for (int e = tid; e < NR * 16; e += kSoft) {
+        const int row = e >> 4, ch = e & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < p.R) {
+          const int t = row / group;
+          const int hq = g.hkv * group + row % group;
+          v = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + ch);
+        }
+        *reinterpret_cast<uint4 *>(sQ + (ch >> 3) * (NR * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    named_bar_arrive(kBarQ, kSoft + 32);
+
+    // ---- draft visibility: loads issued now, masks built before the first draft tile ----
+    DraftPre dpre{-1, -1, 0ull, 0ull};
+    if (warp == 0 && lt1 * TK > g.n_prefix) dpre = draft_prefetch(p, g.b);
+    bool masks_ready = false;
+
+    float mu[NR];  // reference max per row, log2 units
+#pragma unroll
+    for (int r = 0; r < NR; ++r) mu[r] = -INFINITY;
+
+    for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
+      const int b = jt & 1;
+      const int st = it % NS;
+      const uint32_t tS = tO + (2 + b) * NC;
+      const int key = lt * TK + tid;
+      const bool masked = lt * TK + TK > g.n_prefix;
+      if (masked && !masks_ready) {
+        // per draft key dk, the packed rows r = t * group + h of the tokens t that see it
+        if (warp == 0) {
+          uint64_t lo, hi;
+          draft_rows(p, dpre, lo, hi);
+          if (lane < p.T) rowmask[lane] = lo;
+          if (lane + 32 < p.T) rowmask[lane + 32] = hi;
+        }
+        named_bar_sync(kBarSoft, kSoft);
+        if (tid < p.T) {
+          const uint64_t gbits = group >= 64 ? ~0ull : ((1ull << group) - 1);
+          uint64_t kmask = 0;
+          for (int t = 0; t < p.T; ++t)
+            if ((rowmask[t] >> tid) & 1ull) kmask |= gbits << (t * group);
+          keymask[tid] = kmask;
+        }
+        named_bar_sync(kBarSoft, kSoft);
+        masks_ready = true;
+      }
+      uint64_t km = ~0ull;  // rows that see this key
+      if (masked) {
+        if (key >= g.nkeys) km = 0;
+        else if (key >= g.n_prefix) km = keymask[key - g.n_prefix];
+      }
+      wait_ok(s_full + b, (uint32_t)(jt >> 1) & 1u);
+      // PV of tile jt-2 (same o_done barrier): waiting for every PV in order,
+      // two tiles late, keeps each barrier at most one phase ahead of its waiter
+      if (jt >= 2) wait_ok(o_done + b, (uint32_t)((jt - 2) >> 1) & 1u);
+      tc_fence_after();
+      float x[NR];  // raw scores of this key, -inf where the row does not see it
+      auto load_scores = [&]() {
+        tmem_ld_f<NR>(tS, x);
+        if (masked) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r)
+            if (!((km >> r) & 1ull)) x[r] = -INFINITY;
+        }
+      };
+      load_scores();
+      if (lt == lt0) {
+        // first tile of this part: the scores of key 0 are the reference; the
+        // vote below moves it to the exact maxima only when some score is more
+        // than 2^8 above it (or key 0 is hidden from a row)
+        if (tid == 0) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) reinterpret_cast<float *>(red)[r] = x[r] * cl2;
+        }
+        named_bar_sync(kBarRed, kSoft);
+#pragma unroll
+        for (int r = 0; r < NR; r += 4) {
+          const float4 m4 = reinterpret_cast<const float4 *>(red)[r >> 2];
+          mu[r] = m4.x;
+          mu[r + 1] = m4.y;
+          mu[r + 2] = m4.z;
+          mu[r + 3] = m4.w;
+        }
+      }
+      float dmax = -INFINITY;  // (NaN where a row has seen nothing yet: ignored by fmaxf)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, fmaf(x[r], cl2, -mu[r]));
+      if (bar_red_or(kBarRed, kSoft, dmax > 8.f)) {
+        // some score passed its reference by more than 2^8: move the references
+        // to the exact row maxima seen so far
+        WarpScatterMax<NR, 16>::run(x, lane);
+        if constexpr (NR >= 32) {
+#pragma unroll
+          for (int j = 0; j < NR / 32; ++j) reinterpret_cast<float *>(red)[(j + (NR / 32) * lane) * 4 + warp] = x[j];
+        } else {
+          if ((lane & (32 / NR - 1)) == 0) reinterpret_cast<float *>(red)[(lane / (32 / NR)) * 4 + warp] = x[0];
+        }
+        named_bar_sync(kBarRed, kSoft);
+        float *alpha = x;  // the scores are reloaded below
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const float4 m4 = red[r];
+          const float mnew = fmaxf(mu[r], fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)) * cl2);
+          alpha[r] = mu[r] == -INFINITY ? 0.f : ex2_approx(mu[r] - mnew);
+          mu[r] = mnew;
+        }
+        if (lt != lt0) {
+          wait_ok(o_done + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);  // O and l hold every PV up to tile jt-1
+          tc_fence_after();
+          tmem_scale_cols<NR>(tO, x);
+          tmem_scale_cols<NR>(tL, x);
+          tmem_st_wait();
+        }
+        load_scores();
+      }
+      // P^T row of this key over the K tile of the stage (the S MMA is done with it)
+      uint8_t *pk = stages + st * SM::kStageBytes;
+      const int sw = tid & 7;
+      if (masked) {
+#pragma unroll
+        for (int cc = 0; cc < NR / 8; ++cc) {
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = 8 * cc + 2 * q;
+            // a row that has seen no key yet has mu = -inf and only -inf scores: P = 0
+            const float a = ex2_approx(fmaf(x[r], cl2, mu[r] == -INFINITY ? 0.f : -mu[r]));
+            const float bq = ex2_approx(fmaf(x[r + 1], cl2, mu[r + 1] == -INFINITY ? 0.f : -mu[r + 1]));
+            split_bf16x2(a, bq, h[q], l[q]);
+          }
+          const int off = tid * 128 + ((cc ^ sw) << 4);
+          *reinterpret_cast<uint4 *>(pk + off) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4 *>(pk + TK * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+        if (use_tma && key >= g.nkeys) {
+          // rows past the segment end: TMA brought whatever follows; zero V so 0 * V stays 0
+          wait_ok(full + st, (uint32_t)(it / NS) & 1u);
+          uint8_t *vt = pk + Geo::kTileBytes;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) *reinterpret_cast<uint4 *>(vt + swz<TK>(tid, ch)) = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        // every row sees every key of a prefix tile, so mu is finite here
+#pragma unroll
+        for (int cc = 0; cc < NR / 8; ++cc) {
+          uint32_t h[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = 8 * cc + 2 * q;
+            h[q] = pack_bf16(ex2_approx(fmaf(x[r], cl2, -mu[r])), ex2_approx(fmaf(x[r + 1], cl2, -mu[r + 1])));
+          }
+          *reinterpret_cast<uint4 *>(pk + tid * 128 + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full + b);
+    }
+
+    // ---- epilogue: column d = tid of O / l for every row of this segment part ----
+    if (jt >= 2) wait_ok(o_done + (jt & 1), (uint32_t)((jt - 2) >> 1) & 1u);
+    wait_ok(o_done + ((jt - 1) & 1), (uint32_t)((jt - 1) >> 1) & 1u);
+    tc_fence_after();
+    constexpr int CH = NR < 32 ? NR : 32;  // columns per TMEM load
+    const size_t slot = (size_t)(s + c);
+    // per-row constants, once: thread r takes row r (l is the same on every
+    // lane); its l and reference max are picked out of the register arrays by
+    // predicated selects, so the rows are done by the threads in parallel
+    float my_l = 0.f, my_mu = 0.f;
+#pragma unroll
+    for (int h = 0; h < NR / CH; ++h) {
+      float lv[CH];
+      tmem_ld_f<CH>(tL + h * CH, lv);
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        my_l = tid == h * CH + j ? lv[j] : my_l;
+        my_mu = tid == h * CH + j ? mu[h * CH + j] : my_mu;
+      }
+    }
+    if (tid < p.R) {
+      const int r = tid;
+      const int t = r / group;
+      const int hq = g.hkv * group + r % group;
+      const float lse_nat = my_l > 0.f ? (my_mu + __log2f(my_l)) * kLn2 : -INFINITY;
+      row_inv[r] = my_l > 0.f ? __fdividef(1.f, my_l) : 0.f;
+      if (ok) {
+        if (n_parts == 1)
+          p.lse[((size_t)g.b * p.Hq + hq) * p.T + t] = lse_nat;
+        else
+          p.lse_part[slot * p.rows_pad + r] = lse_nat;
+      }
+    }
+    named_bar_sync(kBarSoft, kSoft);
+    // column d = tid of O / l for every row, staged row-major in the Q buffer
+    // (free: every MMA of this part has completed) and written by bulk copies
+    if (n_parts > 1) {
+      // fp32 part: the slot's NR rows are contiguous; two halves of NR/2 rows
+      constexpr int HR = NR / 2;
+      float *stage_f = reinterpret_cast<float *>(sQ);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float ov[HR];
+        tmem_ld_f<HR>(tO + half * HR, ov);
+#pragma unroll
+        for (int j = 0; j < HR; j += 4) {
+          const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + half * HR + j);
+          stage_f[(j + 0) * D + tid] = ov[j] * inv4.x;
+          stage_f[(j + 1) * D + tid] = ov[j + 1] * inv4.y;
+          stage_f[(j + 2) * D + tid] = ov[j + 2] * inv4.z;
+          stage_f[(j + 3) * D + tid] = ov[j + 3] * inv4.w;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kBarSoft, kSoft);
+        if (tid == 0 && ok) {
+          bulk_store_s2g(p.o_part + (slot * p.rows_pad + half * HR) * D, stage_f, (uint32_t)(HR * D * 4));
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        named_bar_sync(kBarSoft, kSoft);
+      }
+    } else {
+      // final bf16 rows: the group rows of one draft token are contiguous in out
+      __nv_bfloat16 *stage_b = reinterpret_cast<__nv_bfloat16 *>(sQ);
+#pragma unroll
+      for (int h = 0; h < NR / CH; ++h) {
+        float ov[CH];
+        tmem_ld_f<CH>(tO + h * CH, ov);
+#pragma unroll
+        for (int j = 0; j < CH; j += 4) {
+          const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + h * CH + j);
+          stage_b[(h * CH + j + 0) * D + tid] = __float2bfloat16_rn(ov[j] * inv4.x);
+          stage_b[(h * CH + j + 1) * D + tid] = __float2bfloat16_rn(ov[j + 1] * inv4.y);
+          stage_b[(h * CH + j + 2) * D + tid] = __float2bfloat16_rn(ov[j + 2] * inv4.z);
+          stage_b[(h * CH + j + 3) * D + tid] = __float2bfloat16_rn(ov[j + 3] * inv4.w);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kBarSoft, kSoft);
+      if (ok && tid < p.T) {
+        const int t = tid;
+        __nv_bfloat16 *dst =
+            static_cast<__nv_bfloat16 *>(p.out) + (((size_t)g.b * p.T + t) * p.Hq + g.hkv * group) * D;
+        const __nv_bfloat16 *src = stage_b + (size_t)t * group * D;
+        if (p.out_align16) {
+          bulk_store_s2g(dst, src, (uint32_t)(group * D * 2));
+          bulk_commit();
+          bulk_wait_read_all();
+        } else {
+          for (int e = 0; e < group * D; ++e) dst[e] = src[e];
+        }
+      }
+      named_bar_sync(kBarSoft, kSoft);
+    }
+  }
+  // the output and part rows written by bulk copies have landed
+  bulk_wait_all();
+  // the combine kernel may start once every CTA has written its parts
+  pdl_launch_dependents();
+  tc_fence_before();
+  named_bar_sync(kBarEnd, kSoft + 32);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int NR>
+static size_t tck_smem_bytes(int S) {
+  return 1024 + (size_t)TkSmem<NR>::kTstartOff + (size_t)(S + 1) * 4;
+}
+
+size_t attn_tck_smem_required(const AttnParams &p) {
+  return p.rows_pad <= 16 ? tck_smem_bytes<16>(p.S) : p.rows_pad <= 32 ? tck_smem_bytes<32>(p.S)
+                                                                       : tck_smem_bytes<64>(p.S);
+}
+
+template <int NR>
+static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                cudaStream_t stream) {
+  const size_t smem = tck_smem_bytes<NR>(p.S);
+  auto kern = verify_attn_tck_kernel<NR>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTkThreads, smem, stream>>>(p, tmk, tmv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                 cudaStream_t stream) {
+  if (p.rows_pad <= 16) return launch_tck_t<16>(p, tmk, tmv, grid, stream);
+  if (p.rows_pad <= 32) return launch_tck_t<32>(p, tmk, tmv, grid, stream);
+  return launch_tck_t<64>(p, tmk, tmv, grid, stream);
+}
+
+}  // namespace va

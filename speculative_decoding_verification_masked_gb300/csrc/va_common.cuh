@@ -126,6 +126,19 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Bulk copy shared -> global (16-byte aligned addresses, size a multiple of
+// 16), tracked as a bulk group of the issuing thread.
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the sources of this thread's bulk groups have been read (the shared memory may be reused)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk groups have completed (their global writes are performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {

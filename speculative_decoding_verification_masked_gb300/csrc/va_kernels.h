@@ -18,7 +18,8 @@ struct AttnParams {
   int NRB;     // row blocks per (sequence, kv-head)
   int S;       // segments = B * Hkv * NRB
   int rows_pad;// rows per segment slot in the partial buffers
-  int use_tc;  // 1: tcgen05 kernel (bf16, D 128, more than 64 packed rows)
+  int use_tc;  // tcgen05 kernels (bf16, D 128): 1 = rows on TMEM lanes (more than 64
+              // packed rows), 2 = keys on TMEM lanes (at most 64); 0 = mma.sync kernel
   int cps;     // CTAs of the attention kernel resident per SM (1 or 2)
   float scale;
   va_dtype dtype;
@@ -36,6 +37,7 @@ struct AttnParams {
   int mask_words;
   // outputs
   void *out;
+  int out_align16;  // out is 16-byte aligned (bulk copies allowed)
   float *lse;
   // workspace
   int *status;
@@ -48,6 +50,9 @@ size_t attn_smem_required(const AttnParams &p);
 size_t attn_tc_smem_required(const AttnParams &p);
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream);
+size_t attn_tck_smem_required(const AttnParams &p);
+cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                 cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                              cudaStream_t stream);
 cudaError_t launch_combine_generic(int n_rows, int n_parts, int D, const float *o_parts, const float *lse_parts,

@@ -16,23 +16,24 @@ constexpr int kTK = 64;  // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Geometry of one stage of the ring: a 64-key K tile and V tile, each split in
-// 128-byte columns of 64 swizzled rows.
-template <typename Tin, int D>
+// Geometry of one stage of the ring: a TK-key K tile and V tile, each split in
+// 128-byte columns of TK swizzled rows.
+template <typename Tin, int D, int TK = kTK>
 struct StageGeom {
   static constexpr int kRowBytes = D * (int)sizeof(Tin);  // 128 or 256
   static constexpr int kChunks = kRowBytes / 16;          // 16-byte chunks per row
   static constexpr int kHalves = kRowBytes / 128;         // 128-byte swizzle columns per row
-  static constexpr int kTileBytes = kHalves * kTK * 128;  // one 64-key tile of K (or V)
+  static constexpr int kTileBytes = kHalves * TK * 128;   // one TK-key tile of K (or V)
   static constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
 };
 
-// Byte offset of 16-byte chunk c of key row r inside a tile: rows are split in
-// 128-byte columns (c / 8) of 64 rows each, and inside a column the chunk index
-// is XORed with r % 8 -- the TMA 128-byte swizzle, which also makes every
-// 8-row ldmatrix conflict-free.
+// Byte offset of 16-byte chunk c of key row r inside a TK-row tile: rows are
+// split in 128-byte columns (c / 8) of TK rows each, and inside a column the
+// chunk index is XORed with r % 8 -- the TMA 128-byte swizzle, which also makes
+// every 8-row ldmatrix conflict-free.
+template <int TK = kTK>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)((c >> 3) * (kTK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  return (uint32_t)((c >> 3) * (TK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 // ---------------------------------------------------------------------------
@@ -102,14 +103,13 @@ __device__ __forceinline__ int owner_cta(long long t, long long total, int G) {
 // ---------------------------------------------------------------------------
 // draft visibility of one draft token t as a 64-bit row (bit j = draft key j)
 // ---------------------------------------------------------------------------
-// Ancestor-or-self rows for t = lane and t = lane + 32, computed by the whole
-// warp from parent pointers (LongSpec 1.3 / 2.C: a tree node sees its path).
-__device__ __forceinline__ void warp_tree_rows(const AttnParams &p, int b, uint64_t &row_lo, uint64_t &row_hi) {
+// Ancestor-or-self rows for t = lane and t = lane + 32 from the parents of
+// those nodes (p_lo, p_hi; -1 past T), walked by the whole warp with shuffles
+// (LongSpec 1.3 / 2.C: a tree node sees its path).
+__device__ __forceinline__ void warp_tree_walk(const AttnParams &p, int p_lo, int p_hi, uint64_t &row_lo,
+                                               uint64_t &row_hi) {
   const int lane = threadIdx.x & 31;
   const int T = p.T;
-  const int32_t *par = p.parent + (size_t)b * T;
-  int p_lo = lane < T ? __ldg(par + lane) : -1;
-  int p_hi = lane + 32 < T ? __ldg(par + lane + 32) : -1;
   // a parent that breaks -1 <= parent[i] < i ends the path at that node
   if (p_lo < -1 || p_lo >= lane) {
     if (lane < T) record_status(p.status, VA_ERR_DEVICE_BOUNDS);
@@ -135,6 +135,59 @@ __device__ __forceinline__ void warp_tree_rows(const AttnParams &p, int b, uint6
   }
   row_lo = r0;
   row_hi = r1;
+}
+
+__device__ __forceinline__ void warp_tree_rows(const AttnParams &p, int b, uint64_t &row_lo, uint64_t &row_hi) {
+  const int lane = threadIdx.x & 31;
+  const int32_t *par = p.parent + (size_t)b * p.T;
+  const int p_lo = lane < p.T ? __ldg(par + lane) : -1;
+  const int p_hi = lane + 32 < p.T ? __ldg(par + lane + 32) : -1;
+  warp_tree_walk(p, p_lo, p_hi, row_lo, row_hi);
+}
+
+// The draft structure of sequence b for rows t = lane and lane + 32, loaded
+// ahead of use (parents, or the rows of an explicit bitmask).
+struct DraftPre {
+  int p_lo, p_hi;
+  uint64_t w_lo, w_hi;
+};
+
+__device__ __forceinline__ DraftPre draft_prefetch(const AttnParams &p, int b) {
+  const int lane = threadIdx.x & 31;
+  DraftPre d;
+  d.p_lo = d.p_hi = -1;
+  d.w_lo = d.w_hi = 0;
+  if (p.parent != nullptr) {
+    const int32_t *par = p.parent + (size_t)b * p.T;
+    if (lane < p.T) d.p_lo = __ldg(par + lane);
+    if (lane + 32 < p.T) d.p_hi = __ldg(par + lane + 32);
+  } else if (p.mask != nullptr) {
+    const uint32_t *w = p.mask + (size_t)b * p.T * p.mask_words;
+    if (lane < p.T) {
+      d.w_lo = __ldg(w + (size_t)lane * p.mask_words);
+      if (p.mask_words > 1) d.w_lo |= (uint64_t)__ldg(w + (size_t)lane * p.mask_words + 1) << 32;
+    }
+    if (lane + 32 < p.T) {
+      d.w_hi = __ldg(w + (size_t)(lane + 32) * p.mask_words);
+      if (p.mask_words > 1) d.w_hi |= (uint64_t)__ldg(w + (size_t)(lane + 32) * p.mask_words + 1) << 32;
+    }
+  }
+  return d;
+}
+
+// Visibility rows of draft tokens t = lane and lane + 32 (whole warp).
+__device__ __forceinline__ void draft_rows(const AttnParams &p, const DraftPre &d, uint64_t &row_lo,
+                                           uint64_t &row_hi) {
+  const int lane = threadIdx.x & 31;
+  if (p.parent != nullptr) {
+    warp_tree_walk(p, d.p_lo, d.p_hi, row_lo, row_hi);
+  } else if (p.mask != nullptr) {
+    row_lo = d.w_lo;
+    row_hi = d.w_hi;
+  } else {  // causal chain
+    row_lo = (2ull << lane) - 1;
+    row_hi = lane + 32 >= 63 ? ~0ull : ((2ull << (lane + 32)) - 1);
+  }
 }
 
 // Visibility row of draft token t for sequence b.  Must be called by a full
@@ -195,12 +248,13 @@ struct CtaRange {
   int s0;           // first segment touching t0
 };
 
-// Tiles per segment, their exclusive scan into tstart[0..S], and this CTA's
-// range.  Called by every thread of the block (contains __syncthreads).
+// Tiles of TK keys per segment, their exclusive scan into tstart[0..S], and
+// this CTA's range.  Called by every thread of the block (contains __syncthreads).
+template <int TK = kTK>
 __device__ __forceinline__ CtaRange plan_cta(const AttnParams &p, int *tstart) {
   for (int s = threadIdx.x; s < p.S; s += blockDim.x) {
     const Seg g = seg_info(p, s, true);
-    tstart[s] = (g.nkeys + kTK - 1) / kTK;
+    tstart[s] = (g.nkeys + TK - 1) / TK;
   }
   __syncthreads();
   if ((threadIdx.x >> 5) == 0) warp_scan_inplace(tstart, p.S);
@@ -232,12 +286,18 @@ __device__ __forceinline__ CtaRange plan_cta(const AttnParams &p, int *tstart) {
 // full[st] completes when stage st holds the tile (TMA: one expect_tx arrive
 // plus the box bytes; cp.async: one arrive per lane); empty[st] is completed by
 // the consumers when they are done with it.  Returns the tiles issued.
-template <typename Tin, int D, int NS>
+// At most MAXF tiles are in flight (issued, not landed): tile j is issued
+// once tile j - MAXF has landed, and with a cap the second tile waits for the
+// first, so at the start of the kernel the first tile of every CTA does not
+// share the memory system with the rest of the ring.
+template <typename Tin, int D, int NS, int TK = kTK, int MAXF = NS>
 __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                              const int *tstart, const CtaRange &cr, uint8_t *stages,
                                              uint64_t *full, uint64_t *empty, volatile int *abort_flag,
                                              bool use_tma, bool &ok) {
-  using C = StageGeom<Tin, D>;
+  using C = StageGeom<Tin, D, TK>;
+  constexpr int kBox = 64;          // rows of one TMA box
+  constexpr int kRowSets = TK / 32; // key rows per lane in the gather
   const int lane = threadIdx.x & 31;
   const uint64_t policy = l2_evict_first_policy();
   const Tin *kbase = static_cast<const Tin *>(p.k);
@@ -260,37 +320,56 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
         *abort_flag = 1;
         ok = false;
       }
+      // (with a cap, the second tile also waits for the first, which then lands sooner)
+      const int gate = it >= MAXF ? it - MAXF : (it == 1 ? 0 : -1);
+      if (MAXF < NS && ok && gate >= 0 &&
+          !mbar_wait(full + gate % NS, (uint32_t)(gate / NS) & 1u, p.wait_ns)) {
+        record_status(p.status, VA_ERR_TIMEOUT);
+        *abort_flag = 1;
+        ok = false;
+      }
       if (!ok) continue;
       uint8_t *kdst = stages + st * C::kStageBytes;
       uint8_t *vdst = kdst + C::kTileBytes;
-      const int k0 = lt * kTK;
+      const int k0 = lt * TK;
       if (use_tma) {
-        // dense: 64 consecutive tokens of this kv-head, one box per 128-byte column;
-        // rows past the segment end arrive too (other tokens or zero fill) and are masked
+        // dense: TK consecutive tokens of this kv-head, boxes of 64 rows per
+        // 128-byte column; rows past the segment end arrive too (other tokens
+        // or zero fill) and are masked
         if (lane == 0) {
           mbar_arrive_expect_tx(full + st, (uint32_t)C::kStageBytes);
           const int row0 = g.b * p.len_cap + k0;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
-            tma_load_3d(kdst + h * kTK * 128, tmk, h * (128 / (int)sizeof(Tin)), g.hkv, row0, full + st, policy);
-            tma_load_3d(vdst + h * kTK * 128, tmv, h * (128 / (int)sizeof(Tin)), g.hkv, row0, full + st, policy);
+#pragma unroll
+            for (int rb = 0; rb < TK / kBox; ++rb) {
+              const int off = h * TK * 128 + rb * kBox * 128;
+              tma_load_3d(kdst + off, tmk, h * (128 / (int)sizeof(Tin)), g.hkv, row0 + rb * kBox, full + st, policy);
+              tma_load_3d(vdst + off, tmv, h * (128 / (int)sizeof(Tin)), g.hkv, row0 + rb * kBox, full + st, policy);
+            }
           }
         }
       } else {
         // paged / sparse: gather rows with 16-byte copies; rows past the end are zero-filled
-        const Tin *r0 = (k0 + lane < g.nkeys) ? key_row<Tin, D>(p, g, k0 + lane, kbase) : kbase;
-        const Tin *r1 = (k0 + lane + 32 < g.nkeys) ? key_row<Tin, D>(p, g, k0 + lane + 32, kbase) : kbase;
+        const Tin *rows[kRowSets];
+#pragma unroll
+        for (int j = 0; j < kRowSets; ++j)
+          rows[j] = (k0 + lane + 32 * j < g.nkeys) ? key_row<Tin, D>(p, g, k0 + lane + 32 * j, kbase) : kbase;
         constexpr int CPR = C::kChunks;  // lanes per row
         constexpr int RPP = 32 / CPR;    // rows per pass
         const int cc = lane % CPR;
 #pragma unroll 4
-        for (int i = 0; i < kTK / RPP; ++i) {
+        for (int i = 0; i < TK / RPP; ++i) {
           const int r = i * RPP + lane / CPR;
-          const uint64_t a = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(r0), r & 31);
-          const uint64_t b = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(r1), r & 31);
-          const uintptr_t src = (uintptr_t)(r < 32 ? a : b) + (uintptr_t)cc * 16u;
+          uint64_t a = 0;
+#pragma unroll
+          for (int j = 0; j < kRowSets; ++j) {
+            const uint64_t x = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(rows[j]), r & 31);
+            if ((r >> 5) == j) a = x;
+          }
+          const uintptr_t src = (uintptr_t)a + (uintptr_t)cc * 16u;
           const uint32_t n = (k0 + r < g.nkeys) ? 16u : 0u;
-          const uint32_t off = swz(r, cc);
+          const uint32_t off = swz<TK>(r, cc);
           cp_async_16(kdst + off, reinterpret_cast<const void *>(src), n);
           cp_async_16(vdst + off, reinterpret_cast<const void *>(src + vdelta), n);
         }

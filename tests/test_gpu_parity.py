@@ -69,11 +69,37 @@ def test_tiny_config_full():
         assert eo < 1e-4 and el < 1e-4  # fp32 path, no TF32
 
 
-@pytest.mark.parametrize("L", [0, 1, 63, 64, 1000, 4099])
+@pytest.mark.parametrize("L", [0, 1, 63, 64, 120, 125, 128, 1000, 4099])
 def test_chain_small(L):
+    """Prefix lengths around the 64- and 128-key tile edges: the draft block
+    inside one tile, straddling two, or starting a tile of its own."""
     w = W.make_workload("chain", seed=L, L=L)
     for mode in ("parent", "causal", "mask"):
         _check(w, mode)
+
+
+@pytest.mark.parametrize("case", ["chain", "paged", "shapes", "empty_row"])
+def test_small_rows_on_mma_kernel(case, monkeypatch):
+    """Segments of at most 64 rows with d128 run on the keys-on-lanes tcgen05
+    kernel by default; VA_SMALL_ROWS_KERNEL=mma routes them to the mma.sync
+    kernel, which stays held to the same bar."""
+    monkeypatch.setenv("VA_SMALL_ROWS_KERNEL", "mma")
+    if case == "chain":
+        for L in (0, 125, 4099):
+            _check(W.make_workload("chain", seed=L, L=L), "parent")
+    elif case == "paged":
+        _check(W.make_workload("paged", seed=21, B=4, L_lo=40, L_hi=700, page_size=16), "mask")
+    elif case == "shapes":
+        for Hq, Hkv, T in ((8, 8, 3), (16, 2, 8), (12, 4, 7)):
+            _check(W.make_workload("tree", seed=Hq * T, Hq=Hq, Hkv=Hkv, T=T, D=128, L=517, tree="random", B=2),
+                   "parent")
+    else:
+        w0 = W.make_workload("tree", seed=10, B=2, T=12, L=0, tree="random_mask", density=0.3)
+        m = w0.mask_words.copy()
+        m[0, 5, 0] = 0
+        w0.mask_words = m
+        out, lse = run_library(w0, "mask")
+        compare(out, lse, oracle.verify(w0))
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -85,13 +111,32 @@ def test_tree_small(seed):
 
 @pytest.mark.parametrize("Hq,Hkv,T,D", [(8, 8, 3, 128), (16, 2, 8, 128), (32, 8, 5, 64), (4, 1, 64, 64),
                                         (12, 4, 7, 128), (32, 2, 9, 128), (32, 4, 16, 128), (20, 2, 10, 128),
-                                        (32, 8, 64, 128), (16, 1, 40, 128)])
+                                        (32, 8, 64, 128), (16, 1, 40, 128), (2, 2, 40, 128), (6, 2, 11, 128),
+                                        (4, 1, 4, 128)])
 def test_shapes_and_row_blocks(Hq, Hkv, T, D):
-    """group*T from 3 to 640 rows: the mma.sync kernel with 1, 2, 4 row groups and
-    several row blocks, and the tcgen05 kernel with one or two 128-row M-tiles,
-    padded rows and several 256-row blocks."""
+    """group*T from 3 to 640 rows: d64 on the mma.sync kernel with 1, 2, 4 row
+    groups; d128 up to 64 rows on the keys-on-lanes tcgen05 kernel (16, 32 and
+    64 row columns, padded), above that on the rows-on-lanes tcgen05 kernel with
+    one or two 128-row M-tiles and several 256-row blocks."""
     w = W.make_workload("tree", seed=Hq * T, Hq=Hq, Hkv=Hkv, T=T, D=D, L=517, tree="random", B=2)
     _check(w, "parent")
+
+
+@pytest.mark.parametrize("offset", [0, 4])
+def test_whole_segments_and_output_alignment(offset):
+    """192 one-tile segments: each is whole inside one CTA, which writes the final
+    rows itself (bulk copies when out is 16-byte aligned, plain stores at an
+    8-byte offset) with no merge."""
+    w = W.make_workload("chain", seed=30 + offset, B=24, L_lo=40, L_hi=110, tree="random")
+    ref = oracle.verify(w)
+    q = w.q.cuda()
+    flat = torch.zeros(q.numel() + offset, dtype=q.dtype, device="cuda")
+    out = flat[offset:].view(q.shape)
+    assert (out.data_ptr() % 16 == 0) == (offset == 0)
+    o, lse = va.verify_attn_dense(q, w.k_cache.cuda(), w.v_cache.cuda(), dev_i32(w.seqlens),
+                                  tree_parent=dev_i32(w.parent), out=out)
+    torch.cuda.synchronize()
+    compare(o, lse, ref)
 
 
 def test_random_masks_and_empty_rows():
