@@ -95,8 +95,8 @@ typedef struct {
  * device (it depends on the device's SM count).  0 on invalid shape. */
 size_t verify_attn_workspace_size(const va_shape *shape);
 
-/* Clear the workspace's status word and bookkeeping (enqueued on `stream`).
- * Call once after allocating a workspace and after an error status. */
+/* Initialise a workspace: status word and merge bookkeeping (on `stream`).
+ * Zeroes all ws_bytes; call once after allocating a workspace. */
 va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream stream);
 
 /*

@@ -249,6 +249,10 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   uint8_t *ws = static_cast<uint8_t *>(c.ws);
   p.status = reinterpret_cast<int *>(ws);
   p.meta = reinterpret_cast<int2 *>(ws + wl.meta_off);
+  p.split_list = reinterpret_cast<int4 *>(ws + wl.split_off);
+  p.split_count = reinterpret_cast<int *>(ws + va::kSplitCountOff);
+  p.split_done = reinterpret_cast<int *>(ws + va::kSplitDoneOff);
+  p.merge_cnt = reinterpret_cast<int2 *>(ws + wl.mcnt_off);
   p.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
   p.o_part = reinterpret_cast<float *>(ws + wl.o_off);
   p.wait_ns = wait_limit_ns();
@@ -289,7 +293,9 @@ size_t verify_attn_workspace_size(const va_shape *shape) {
 va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream stream) {
   if (workspace == nullptr || ws_bytes < va::kHeaderBytes) return fail(VA_ERR_WORKSPACE, "workspace too small");
   if (!aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  cudaError_t e = cudaMemsetAsync(workspace, 0, va::kHeaderBytes, (cudaStream_t)stream);
+  // all of it: the status word and the merge counters start at zero (the
+  // calls return the counters to zero themselves)
+  cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace init");
   return ok();
 }
@@ -406,7 +412,8 @@ va_status verify_attn_check_status(void *workspace, va_stream stream) {
   e = cudaMemcpy(&status, workspace, sizeof status, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (status != 0) {
-    e = cudaMemset(workspace, 0, sizeof status);
+    // the merge bookkeeping of a call that stopped early is reset with the status
+    e = cudaMemset(workspace, 0, va::kHeaderBytes);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
     switch (status) {
       case VA_ERR_TIMEOUT:

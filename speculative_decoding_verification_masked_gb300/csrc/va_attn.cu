@@ -119,7 +119,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int lt1 = min(tstart[s + 1], t1) - tstart[s];
     const int first_cta = owner_cta(tstart[s], total, G);
     const int n_parts = owner_cta(tstart[s + 1] - 1, total, G) - first_cta + 1;
-    if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
+    if (lt0 == 0 && tid == 0) {
+      p.meta[s] = make_int2(s + first_cta, n_parts);
+      if (n_parts > 1)  // one entry per split segment
+        p.split_list[atomicAdd(p.split_count, 1)] = make_int4(s, s + first_cta, n_parts, 0);
+    }
     const bool has_draft = lt1 * kTK > g.n_prefix;
     uint64_t tl = 0, th = 0;
     if (has_draft && p.parent != nullptr) warp_tree_rows(p, g.b, tl, th);
@@ -602,30 +606,102 @@ __device__ __forceinline__ void combine_row(int n_parts, int D, const float *o, 
   }
 }
 
+// Merge of the segments the attention grid cut over several CTAs (their list
+// is in the workspace).  A block of 128 threads holds 128 / (D/4) row slots;
+// a slot of D/4 lanes merges one packed row, each lane four columns.  The lse
+// and output loads of up to kSplitBatch parts are issued together and merged
+// with a running maximum (exact for any number of parts), so a row costs one
+// round trip per batch.  Blocks stride over (listed segment, row) items; the
+// last block to take a ticket resets the list for the next call.
+constexpr int kSplitBatch = 24;
+
 template <typename OutT>
-__global__ void __launch_bounds__(128) combine_segments_kernel(const AttnParams p) {
-  // wait until every CTA of the attention grid has finished and flushed
-  pdl_wait_primary();
+__device__ __forceinline__ void merge_split_row(const AttnParams &p, int4 e, int row, int li) {
+  const int s = e.x, P = e.z;
   const int D = p.D;
-  const int s = blockIdx.x / p.rows_pad;
-  const int row = blockIdx.x % p.rows_pad;
-  if (s >= p.S) return;
-  const int2 meta = p.meta[s];
-  if (meta.y <= 1) return;
   const int rb = s % p.NRB;
   const int hkv = (s / p.NRB) % p.Hkv;
   const int b = s / (p.NRB * p.Hkv);
   const int rr = rb * p.rows_pad + row;
-  if (rr >= p.R) return;
   const int group = p.Hq / p.Hkv;
   const int t = rr / group;
   const int hq = hkv * group + rr % group;
-  const size_t slot0 = (size_t)meta.x;
-  const float *o = p.o_part + (slot0 * p.rows_pad + row) * D;
-  const float *l = p.lse_part + slot0 * p.rows_pad + row;
-  OutT *out = static_cast<OutT *>(p.out) + (((size_t)b * p.T + t) * p.Hq + hq) * D;
-  float *lse = p.lse + ((size_t)b * p.Hq + hq) * p.T + t;
-  combine_row<OutT>(meta.y, D, o, (size_t)p.rows_pad * D, l, (size_t)p.rows_pad, out, lse);
+  const size_t ostride = (size_t)p.rows_pad * D;
+  const float *o = p.o_part + ((size_t)e.y * p.rows_pad + row) * D + 4 * li;
+  const float *l = p.lse_part + (size_t)e.y * p.rows_pad + row;
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < P; s0 += kSplitBatch) {
+    float ls[kSplitBatch];
+    float4 v[kSplitBatch];
+#pragma unroll
+    for (int j = 0; j < kSplitBatch; ++j) {
+      const bool in = s0 + j < P;
+      ls[j] = in ? __ldg(l + (size_t)(s0 + j) * p.rows_pad) : -INFINITY;
+      v[j] = in ? __ldg(reinterpret_cast<const float4 *>(o + (size_t)(s0 + j) * ostride))
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m = M;
+#pragma unroll
+    for (int j = 0; j < kSplitBatch; ++j) m = fmaxf(m, ls[j]);
+    if (m == -INFINITY) continue;  // no part so far saw a key
+    const float a = M == -INFINITY ? 0.f : __expf(M - m);
+    L *= a;
+    acc.x *= a;
+    acc.y *= a;
+    acc.z *= a;
+    acc.w *= a;
+#pragma unroll
+    for (int j = 0; j < kSplitBatch; ++j) {
+      const float w = ls[j] == -INFINITY ? 0.f : __expf(ls[j] - m);
+      L += w;
+      acc.x = fmaf(w, v[j].x, acc.x);
+      acc.y = fmaf(w, v[j].y, acc.y);
+      acc.z = fmaf(w, v[j].z, acc.z);
+      acc.w = fmaf(w, v[j].w, acc.w);
+    }
+    M = m;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  OutT *out = static_cast<OutT *>(p.out) + (((size_t)b * p.T + t) * p.Hq + hq) * D + 4 * li;
+  store_out<OutT>(out + 0, acc.x * inv);
+  store_out<OutT>(out + 1, acc.y * inv);
+  store_out<OutT>(out + 2, acc.z * inv);
+  store_out<OutT>(out + 3, acc.w * inv);
+  if (li == 0) p.lse[((size_t)b * p.Hq + hq) * p.T + t] = L > 0.f ? M + __logf(L) : -INFINITY;
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(128) combine_segments_kernel(const AttnParams p) {
+  __shared__ int s_count;
+  const int lpr = p.D / 4;    // lanes per row
+  const int spb = 128 / lpr;  // row slots per block
+  const int slot = threadIdx.x / lpr, li = threadIdx.x % lpr;
+  const long long it0 = (long long)blockIdx.x * spb + slot;
+  // wait until every CTA of the attention grid has finished and flushed
+  pdl_wait_primary();
+  // the first item's list entry is read before the list length is known
+  // (the grid never indexes past the list's capacity)
+  int4 e0 = p.split_list[it0 / p.rows_pad];
+  int ticket = 0;
+  if (threadIdx.x == 0) {
+    const int c = *reinterpret_cast<volatile int *>(p.split_count);
+    s_count = c;
+    ticket = atomicAdd(p.split_done, c >= 0 ? 1 : 2);  // taken after the length was read
+  }
+  __syncthreads();
+  const long long items = (long long)s_count * p.rows_pad;
+  for (long long it = it0; it < items; it += (long long)gridDim.x * spb) {
+    const int4 e = it == it0 ? e0 : p.split_list[it / p.rows_pad];
+    const int row = (int)(it % p.rows_pad);
+    if ((e.x % p.NRB) * p.rows_pad + row >= p.R) continue;  // padding row of the last row block
+    merge_split_row<OutT>(p, e, row, li);
+  }
+  // every block took its ticket after reading the length: the last one resets the list
+  if (threadIdx.x == 0 && ticket == (int)gridDim.x - 1) {
+    *p.split_count = 0;
+    *p.split_done = 0;
+  }
 }
 
 template <typename OutT>
@@ -673,7 +749,7 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
   if (p.use_tc == 1) {
     e = launch_attention_tc(p, tmk, tmv, grid, stream);
   } else if (p.use_tc == 2) {
-    e = launch_attention_tck(p, tmk, tmv, grid, stream);
+    return launch_attention_tck(p, tmk, tmv, grid, stream);  // merges its split segments itself
   } else if (p.dtype == VA_DTYPE_FP32) {
     e = launch_attn_t<float, 64, 4>(p, tmk, tmv, grid, stream);
   } else if (p.D == 64) {
@@ -688,9 +764,14 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
   if (e != cudaSuccess) return e;
 
   // combine, chained by programmatic dependent launch
-  const long long rows = (long long)p.S * p.rows_pad;
+  // at most one split segment per CTA boundary: min(S, grid) segments of R rows
+  const int spb = 128 / (p.D / 4);
+  const long long max_items = (long long)min(p.S, grid) * p.rows_pad;
+  long long blocks = (max_items + spb - 1) / spb;
+  const long long cap = 4ll * (grid < 1 ? 1 : grid);
+  if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)rows);
+  cfg.gridDim = dim3((unsigned)(blocks < 1 ? 1 : blocks));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -244,7 +244,11 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     const int lt1 = min(tstart[s + 1], t1) - tstart[s];
     const int first_cta = owner_cta(tstart[s], cr.total, cr.G);
     const int n_parts = owner_cta(tstart[s + 1] - 1, cr.total, cr.G) - first_cta + 1;
-    if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
+    if (lt0 == 0 && tid == 0) {
+      p.meta[s] = make_int2(s + first_cta, n_parts);
+      if (n_parts > 1)  // one entry per split segment
+        p.split_list[atomicAdd(p.split_count, 1)] = make_int4(s, s + first_cta, n_parts, 0);
+    }
 
     // ---- Q of this segment into shared memory (both warpgroups) ----
     named_bar_sync(kBarSoft, kSoftThreads);  // previous segment's MMAs have all completed

@@ -57,7 +57,7 @@ struct TkSmem {
   static constexpr int kBarOff = kQOff + kQBytes;
   // barriers: full[3], empty[3], s_full[2], p_full[2], o_done[2], drain
   static constexpr int kNumBars = 2 * kTkStages + 7;
-  static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // tmem base, abort flag
+  static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // tmem base, abort flag, merge flag
   static constexpr int kRowMaskOff = kMiscOff + 16;        // u64 [64]: draft visibility rows
   static constexpr int kKeyMaskOff = kRowMaskOff + 512;    // u64 [64]: per draft key, rows that see it
   static constexpr int kRedOff = kKeyMaskOff + 512;        // float4 [NR]: per-warp row maxima
@@ -160,6 +160,98 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float *a) 
   }
 }
 
+// Wrapping increments (x = x >= wrap ? 0 : x + 1) of a per-segment merge
+// counter: each of the np parts arrives once (release) and leaves once, so the
+// counter reads >= np once all have arrived and is back at 0 after the last one
+// has left -- no atomic result is waited for.
+__device__ __forceinline__ void red_release_inc_gpu(unsigned *ptr, unsigned wrap) {
+  asm volatile("red.release.gpu.global.inc.u32 [%0], %1;" ::"l"(ptr), "r"(wrap) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_inc_gpu(unsigned *ptr, unsigned wrap) {
+  asm volatile("red.relaxed.gpu.global.inc.u32 [%0], %1;" ::"l"(ptr), "r"(wrap) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Exact log-sum-exp merge (LongSpec 2.C) of rows [r0, r1) of split segment s
+// from its np parts at slots slot0..slot0+np-1, by one warp of n_warps: LPR
+// lanes per row, each with 128/LPR columns, the lse and output loads of up to
+// MB parts in flight at once, a running maximum across batches.
+template <int LPR, int MB>
+__device__ __forceinline__ void merge_rows_warp(const AttnParams &p, int s, int slot0, int np, int r0, int r1,
+                                                int warp_id, int n_warps, int lane) {
+  constexpr int D = 128;
+  constexpr int RPW = 32 / LPR;      // rows per warp pass
+  constexpr int C4 = D / LPR / 4;    // float4 per lane and part
+  const int sub = lane / LPR, li = lane % LPR;
+  const int group = p.Hq / p.Hkv;
+  const int hkv = s % p.Hkv, b = s / p.Hkv;  // one row block per (sequence, kv-head)
+  const size_t ostride = (size_t)p.rows_pad * D;
+  for (int rbase = r0 + warp_id * RPW; rbase < r1; rbase += n_warps * RPW) {
+    const int row = rbase + sub;
+    const bool act = row < r1;
+    const int rr = act ? row : r0;
+    const float *l = p.lse_part + (size_t)slot0 * p.rows_pad + rr;
+    const float *o = p.o_part + ((size_t)slot0 * p.rows_pad + rr) * D + li * C4 * 4;
+    float M = -INFINITY, L = 0.f;
+    float4 acc[C4];
+#pragma unroll
+    for (int c = 0; c < C4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < np; q0 += MB) {
+      float ls[MB];
+      float4 v[MB][C4];
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        const bool in = q0 + j < np;
+        ls[j] = in ? __ldg(l + (size_t)(q0 + j) * p.rows_pad) : -INFINITY;
+#pragma unroll
+        for (int c = 0; c < C4; ++c)
+          v[j][c] = in ? __ldg(reinterpret_cast<const float4 *>(o + (size_t)(q0 + j) * ostride) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float m = M;
+#pragma unroll
+      for (int j = 0; j < MB; ++j) m = fmaxf(m, ls[j]);
+      if (m == -INFINITY) continue;  // no part so far saw a key
+      const float a = M == -INFINITY ? 0.f : __expf(M - m);
+      L *= a;
+#pragma unroll
+      for (int c = 0; c < C4; ++c) {
+        acc[c].x *= a;
+        acc[c].y *= a;
+        acc[c].z *= a;
+        acc[c].w *= a;
+      }
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        const float w = ls[j] == -INFINITY ? 0.f : __expf(ls[j] - m);
+        L += w;
+#pragma unroll
+        for (int c = 0; c < C4; ++c) {
+          acc[c].x = fmaf(w, v[j][c].x, acc[c].x);
+          acc[c].y = fmaf(w, v[j][c].y, acc[c].y);
+          acc[c].z = fmaf(w, v[j][c].z, acc[c].z);
+          acc[c].w = fmaf(w, v[j][c].w, acc[c].w);
+        }
+      }
+      M = m;
+    }
+    if (!act) continue;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int t = row / group, hq = hkv * group + row % group;
+    uint2 *dst = reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                           (((size_t)b * p.T + t) * p.Hq + hq) * D + li * C4 * 4);
+#pragma unroll
+    for (int c = 0; c < C4; ++c)
+      dst[c] = make_uint2(pack_bf16(acc[c].x * inv, acc[c].y * inv), pack_bf16(acc[c].z * inv, acc[c].w * inv));
+    if (li == 0) p.lse[((size_t)b * p.Hq + hq) * p.T + t] = L > 0.f ? M + __logf(L) : -INFINITY;
+  }
+}
+
 template <int NR>
 __global__ void __launch_bounds__(kTkThreads, 1)
     verify_attn_tck_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
@@ -214,17 +306,13 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     fence_mbar_init();
   }
   const CtaRange cr = plan_cta<TK>(p, tstart);  // contains __syncthreads
-  if (c >= cr.G) {
-    pdl_launch_dependents();
-    return;
-  }
+  if (c >= cr.G) return;
   const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
 
   if (warp == kProducerWarp) {
     bool pok = true;
     produce_tiles<__nv_bfloat16, D, NS, TK, 2>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag,
                                                use_tma, pok);
-    pdl_launch_dependents();
     return;
   }
 
@@ -336,7 +424,6 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(SM::kTmemCols)
                  : "memory");
-    pdl_launch_dependents();
     return;
   }
 
@@ -351,6 +438,9 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     tmem_st_wait();
   }
   int it = 0, jt = 0;
+  // split segments this CTA holds a part of (at most its first and its last):
+  // merged after its last tile
+  int n_split = 0, ms[2] = {0, 0}, mslot[2] = {0, 0}, mnp[2] = {0, 0}, mpart[2] = {0, 0};
   for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
     const Seg g = seg_info(p, s, false);
     const int lt0 = max(tstart[s], t0) - tstart[s];
@@ -586,6 +676,21 @@ __global__ void __launch_bounds__(kTkThreads, 1)
         }
         named_bar_sync(kBarSoft, kSoft);
       }
+      // publish the part (always, also after a failed wait, so the counters
+      // return to zero): the block barrier orders every thread's lse stores
+      // before thread 0's release, which follows the landing of the bulk rows
+      named_bar_sync(kBarSoft, kSoft);
+      if (tid == 0) {
+        bulk_wait_all();
+        red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+      }
+      if (n_split < 2) {
+        ms[n_split] = s;
+        mslot[n_split] = s + first_cta;
+        mnp[n_split] = n_parts;
+        mpart[n_split] = c - first_cta;
+        ++n_split;
+      }
     } else {
       // final bf16 rows: the group rows of one draft token are contiguous in out
       __nv_bfloat16 *stage_b = reinterpret_cast<__nv_bfloat16 *>(sQ);
@@ -622,8 +727,38 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   }
   // the output and part rows written by bulk copies have landed
   bulk_wait_all();
-  // the combine kernel may start once every CTA has written its parts
-  pdl_launch_dependents();
+
+  // ---- merge of the split segments: once every part of a segment has
+  // arrived, each of its CTAs merges an equal share of its rows ----
+  volatile int *merge_ok = abort_flag + 1;
+  for (int k = 0; k < n_split; ++k) {
+    const int s = ms[k], np = mnp[k];
+    if (tid == 0) {
+      bool arrived = true;
+      if (ld_acquire_gpu(&p.merge_cnt[s].x) < np) {
+        const uint64_t t0w = globaltimer_ns();
+        while (ld_acquire_gpu(&p.merge_cnt[s].x) < np) {
+          if (globaltimer_ns() - t0w > p.wait_ns) {
+            record_status(p.status, VA_ERR_TIMEOUT);
+            arrived = false;
+            break;
+          }
+        }
+      }
+      *merge_ok = arrived ? 1 : 0;
+    }
+    named_bar_sync(kBarSoft, kSoft);  // thread 0's acquire, then the barrier, orders the reads below
+    if (*merge_ok) {
+      const int r0 = mpart[k] * p.R / np, r1 = (mpart[k] + 1) * p.R / np;
+      if (np <= 4)
+        merge_rows_warp<8, 4>(p, s, mslot[k], np, r0, r1, warp, 4, lane);
+      else
+        merge_rows_warp<32, 24>(p, s, mslot[k], np, r0, r1, warp, 4, lane);
+    }
+    named_bar_sync(kBarSoft, kSoft);
+    // leave: np arrivals and np departures wrap the counter back to zero
+    if (tid == 0) red_relaxed_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * np - 1u);
+  }
   tc_fence_before();
   named_bar_sync(kBarEnd, kSoft + 32);
 }
@@ -648,8 +783,18 @@ static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, con
   auto kern = verify_attn_tck_kernel<NR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kTkThreads, smem, stream>>>(p, tmk, tmv);
-  return cudaGetLastError();
+  // cooperative: every CTA is resident, so the wait for a segment's parts ends
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
 }
 
 cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,

@@ -13,23 +13,33 @@ namespace va {
 
 // ---------------------------------------------------------------------------
 // workspace layout (all offsets 256-byte aligned)
-//   [0, 256)            header: int status word (first device-side error)
+//   [0, 256)            header: int status word (first device-side error) at 0,
+//                       split-list length at kSplitCountOff, merge-blocks-done
+//                       count at kSplitDoneOff (both back to 0 after every merge)
 //   meta   int2[S]      per segment: first partial slot, number of parts
+//   split  int4[slots]  segments cut over more than one CTA (the merge's work
+//                       list): segment, first partial slot, number of parts
+//   mcnt   int2[S]      per segment: the in-kernel merge counter (x; back to 0
+//                       at the end of every call)
 //   lse_p  f32 [slots][rows_pad]
 //   o_p    f32 [slots][rows_pad][D]
 // ---------------------------------------------------------------------------
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kSplitCountOff = 64;
+constexpr size_t kSplitDoneOff = 128;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t meta_off, lse_off, o_off, total;
+  size_t meta_off, split_off, mcnt_off, lse_off, o_off, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int S, int slots, int rows_pad, int D) {
   WsLayout w;
   w.meta_off = kHeaderBytes;
-  w.lse_off = w.meta_off + align256(sizeof(int2) * (size_t)S);
+  w.split_off = w.meta_off + align256(sizeof(int2) * (size_t)S);
+  w.mcnt_off = w.split_off + align256(sizeof(int4) * (size_t)slots);
+  w.lse_off = w.mcnt_off + align256(sizeof(int2) * (size_t)S);
   w.o_off = w.lse_off + align256(sizeof(float) * (size_t)slots * rows_pad);
   w.total = w.o_off + align256(sizeof(float) * (size_t)slots * rows_pad * D);
   return w;

@@ -42,6 +42,9 @@ struct AttnParams {
   // workspace
   int *status;
   int2 *meta;
+  int4 *split_list;              // segments cut over several CTAs: {segment, first slot, parts, 0}
+  int *split_count, *split_done;  // list length; merge blocks done (header words)
+  int2 *merge_cnt;                // per segment: in-kernel merge counter (.x)
   float *lse_part, *o_part;
   uint64_t wait_ns;
 };
@@ -51,6 +54,7 @@ size_t attn_tc_smem_required(const AttnParams &p);
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream);
 size_t attn_tck_smem_required(const AttnParams &p);
+// the keys-on-lanes kernel merges split segments itself (cooperative launch)
 cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,

@@ -299,9 +299,9 @@ def test_workspace_too_small_is_rejected():
 
 @pytest.mark.parametrize("case", ["sparse", "paged_isolated", "dense_ragged"])
 def test_partials_never_read_stale_workspace(case):
-    """Ragged lengths with fewer 64-key tiles than CTAs: every partial slot the
-    combine reads must have been written by this very call.  The workspace is
-    filled with NaN bytes first, so reading a stale slot cannot go unnoticed."""
+    """Ragged lengths with fewer key tiles than CTAs: every partial slot the merge
+    reads must have been written by this very call.  The partial slots hold NaN
+    bytes first, so reading a stale slot cannot go unnoticed."""
     if case == "sparse":
         w = W.make_workload("sparse", seed=3, B=3, L_lo=200, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60)
     elif case == "paged_isolated":
@@ -311,8 +311,10 @@ def test_partials_never_read_stale_workspace(case):
     ref = oracle.verify(w)
     shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0)
     ws = va.Workspace.for_shape(shape)
-    ws.buffer.fill_(0xFF)
+    # initialised (status word and merge counters at zero), then the partial
+    # slots, which fill most of the workspace, overwritten with NaN bytes
     assert va.api.lib().verify_attn_workspace_init(ws.ptr, ws.nbytes, va.api._stream()) == 0
+    ws.buffer[ws.offset + ws.nbytes // 4: ws.offset + ws.nbytes].fill_(0xFF)
     kw = {}
     if w.layout == "sparse":
         kw = dict(indices=dev_i32(ref["indices"]), n_indices=dev_i32(ref["n_indices"]))
