@@ -308,6 +308,50 @@ def cpu_baseline(w, target_s=12.0, max_reps=50):
             "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
 
 
+# DRAM traffic per launch of the dominant kernel, from the committed ncu capture
+# named here (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
+# the sources that kernel is built from are byte-identical to those captured.
+PROFILED_TRAFFIC = {
+    "chain": {"sha256": "15089cccad3cfa6540b5ea18a2167c45c2bdae2fd901bfdf89a5d88943eefb9d", "bytes": 134508544 + 3724032,
+              "summary": "profiles/verify_attn_tck_chain.md"},
+}
+KERNEL_SOURCES = ["va_attn_tck.cu", "va_pipeline.cuh", "va_common.cuh", "va_tcgen05.cuh", "va_kernels.h"]
+
+
+def kernel_sources_sha256():
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_masked_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(config):
+    rec = PROFILED_TRAFFIC.get(config)
+    if rec is None or rec["sha256"] != kernel_sources_sha256():
+        return None
+    return rec["bytes"]
+
+
+def attention_path(w):
+    """Which kernels one verification call launches (mirrors the library's row plan)."""
+    R = (w.Hq // w.Hkv) * w.T
+    small_rows = w.dtype == "bf16" and w.D == 128 and R <= 64 and os.environ.get("VA_SMALL_ROWS_KERNEL") != "mma"
+    if small_rows:
+        nr = 16 if R <= 16 else (32 if R <= 32 else 64)
+        kernel, launches = f"verify_attn_tck_kernel<{nr}> (keys on TMEM lanes, LSE merge inside)", 1
+    elif w.dtype == "bf16" and w.D == 128:
+        kernel, launches = "verify_attn_tc_kernel (rows on TMEM lanes) + split-segment merge kernel", 2
+    else:
+        kernel, launches = "verify_attn_kernel (mma.sync) + split-segment merge kernel", 2
+    if w.layout == "sparse":
+        launches += 1  # the verify-index build
+    return kernel, launches
+
+
 def load_peak_hbm():
     try:
         with open(PEAKS_FILE) as f:
@@ -500,11 +544,11 @@ def main():
         "data": "synthetic (seeded N(0,1) q/k/v, seeded trees/page tables/scores)",
         "config": config_dict(w, main_res["n_copies"]),
         "roofline": {"bound": "hbm", "achieved": round(main_res["call_gbs"], 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(main_res["call_gbs"] / peak, 4), "traffic": None,
-                     "kernel": "verify_attn call (split-KV attention kernel + PDL-chained LSE combine)",
+                     "frac": round(main_res["call_gbs"] / peak, 4), "traffic": profiled_traffic(args.config),
+                     "kernel": attention_path(w)[0],
                      "call_us": round(main_res["call_s"] * 1e6, 3), "peak_kind": peak_kind},
         "e2e": main_res.get("e2e"),
-        "gpu_launches": main_res["steps"] * 2,
+        "gpu_launches": main_res["steps"] * attention_path(w)[1],
         "clocks": main_res["clocks"],
     }
     if "cpu" in main_res:

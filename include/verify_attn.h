@@ -130,7 +130,7 @@ va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_
  * memory.  A shape whose scratch exceeds 8 MiB (verify_attn_workspace_size) is
  * rejected with VA_ERR_UNSUPPORTED before anything is enqueued.  On a 152-SM
  * GPU, d 128 and at most 32 packed query rows per kv-head (GQA group x T),
- * about 200 (sequence, kv-head) pairs fit -- e.g. one sequence with 8 draft
+ * about 350 (sequence, kv-head) pairs fit -- e.g. one sequence with 8 draft
  * tokens, or 16 sequences of 5; a batch of 64 sequences of 16 does not.
  * Sharing.  Every call uses the same array and leaves its contents behind;
  * each call clears the status word it needs.  Calls whose work overlaps on the
