@@ -8,20 +8,25 @@
 //
 // Roles (11 warps when the segment has two 128-row M-tiles):
 //   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
-//                    = one TMEM lane.  Reads S from TMEM, applies the draft
-//                    bitmask, runs the online softmax, writes P (bf16) back
-//                    over S, rescales O in TMEM when the row max grows by
-//                    more than 2^8, and writes the output row.
+//                    = one TMEM lane.  Loads S from TMEM and releases the S
+//                    buffer at once, applies the draft bitmask, runs the online
+//                    softmax, writes P (bf16) into one of two P buffers,
+//                    rescales O in TMEM when the row max grows by more than
+//                    2^8, and writes the output row.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
 //                    sparse) into a 4-stage ring (shared with the other kernel)
 //   warps 4*NMT+1+i  MMA issuer of M-tile i: S_i = Q_i K^T (M128 N64 K128, both
-//                    operands in shared memory, K-major 128B swizzle) into a
-//                    double-buffered TMEM slot, and O_i += P_i V (A = P from
-//                    TMEM, B = V as an MN-major operand).  A chain of dependent
-//                    MMAs issues at MMA latency, so one issuer per M-tile keeps
-//                    two independent chains in the tensor pipe.  Issuer 0 owns
+//                    operands in shared memory, K-major 128B swizzle) into the
+//                    M-tile's S buffer as soon as the softmax has loaded the
+//                    previous S, and O_i += P_i V (A = P from TMEM, B = V as an
+//                    MN-major operand).  P never shares columns with S, so an
+//                    S MMA never overwrites what a running PV MMA reads (MMAs
+//                    with different accumulators are not ordered); only on a
+//                    draft tile, whose bf16 residual of P is parked in the S
+//                    buffer, does the next S wait for the PV.  Issuer 0 owns
 //                    the TMEM allocation.
-// TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
+// TMEM (512 columns): O_i at 128*i, S_i at 256 + 64*i, P_i[b] at
+// 384 + 64*i + 32*b (bf16 pairs).
 // Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
 // barrier sequence of all roles intact, drains and frees TMEM.
 #include <cuda.h>
@@ -45,8 +50,8 @@ struct TcSmem {
   static constexpr int kStageBytes = StageGeom<__nv_bfloat16, 128>::kStageBytes;
   static constexpr int kStagesOff = kQBytes;
   static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
-  // barriers: full[4], empty[4], s_full[2][2], p_full[2][2], o_done[2], drain
-  static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 2 + 1;
+  // barriers: full[4], empty[4], s_full[2], s_free[2], p_full[2][2], o_done[2][2], drain
+  static constexpr int kNumBars = 2 * kTcStages + 2 + 2 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kTstartOff = kMiscOff + 16;
   static constexpr int kThreads = (5 * NMT + 1) * 32;
@@ -77,10 +82,11 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBarOff);
   uint64_t *full = bars;
   uint64_t *empty = bars + NS;
-  uint64_t *s_full = bars + 2 * NS;      // [i][b] at 2*i + b
-  uint64_t *p_full = bars + 2 * NS + 4;  // [i][b]
-  uint64_t *o_done = bars + 2 * NS + 8;  // [i]
-  uint64_t *drain = bars + 2 * NS + 10;
+  uint64_t *s_full = bars + 2 * NS;       // [i]
+  uint64_t *s_free = bars + 2 * NS + 2;   // [i]: the softmax has loaded S_i
+  uint64_t *p_full = bars + 2 * NS + 4;   // [i][b] at 2*i + b, b = tile parity
+  uint64_t *o_done = bars + 2 * NS + 8;   // [i][b]
+  uint64_t *drain = bars + 2 * NS + 12;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
@@ -98,12 +104,14 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       mbar_init(full + i, use_tma ? 1 : 32);
       mbar_init(empty + i, NMT);  // one arrive per M-tile issuer
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(s_free + i, 128);
     }
-    mbar_init(o_done + 0, 1);
-    mbar_init(o_done + 1, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(p_full + i, 128);
+      mbar_init(o_done + i, 1);
+    }
     mbar_init(drain, NMT);
     *abort_flag = 0;
     fence_mbar_init();
@@ -160,33 +168,35 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_s = [&](int i, int b, int st) {  // S_i(b) = Q_i K^T
+    auto issue_s = [&](int i, int st) {  // S_i = Q_i K^T
       if (!ok || lane != 0) return;
       tc_fence_after();
       const uint32_t q0 = smem_u32(sQ) + i * 32768;
       const uint32_t k0 = smem_u32(stages + st * Geo::kStageBytes);
-      const uint32_t dS = tmem + 256 + 64 * (2 * i + b);
+      const uint32_t dS = tmem + 256 + 64 * i;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t a = umma_sdesc(q0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
         const uint64_t bb = umma_sdesc(k0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
         umma_ss(dS, a, bb, id_s, ks > 0);
       }
-      umma_commit(s_full + 2 * i + b);
+      umma_commit(s_full + i);
     };
     auto issue_pv = [&](int i, int b, int st, bool first, bool exact) {  // O_i += P_i V
       if (!ok || lane != 0) return;
       tc_fence_after();
       const uint32_t v0 = smem_u32(stages + st * Geo::kStageBytes + Geo::kTileBytes);
-      const uint32_t aP = tmem + 256 + 64 * (2 * i + b);
+      const uint32_t aP = tmem + 384 + 64 * i + 32 * b;
+      const uint32_t aL = tmem + 256 + 64 * i;  // bf16 residual of P (draft tiles) in the S buffer
       const uint32_t dO = tmem + 128 * i;
 #pragma unroll
       for (int kk = 0; kk < kTK / 16; ++kk) {
         const uint64_t bb = umma_sdesc(v0 + kk * 2048, 8192, 1024);
         umma_ts(dO, aP + kk * 8, bb, id_o, (!first || kk > 0) ? 1u : 0u);
-        if (exact) umma_ts(dO, aP + 32 + kk * 8, bb, id_o, 1u);
+        if (exact) umma_ts(dO, aL + kk * 8, bb, id_o, 1u);
       }
-      umma_commit(o_done + i);
+      umma_commit(o_done + 2 * i + b);
+      umma_commit(empty + st);  // this M-tile is done with the K/V stage once these complete
     };
 
     for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
@@ -195,22 +205,27 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoftThreads + kMmaThreads);  // Q of this segment is in shared memory
       acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
-      issue_s(mi, jt & 1, it % NS);
+      issue_s(mi, it % NS);
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int st = it % NS;
         const int b = jt & 1;
         const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
-        // PV(lt), then -- once it has completed -- S(lt+1) into the other buffer:
-        // no MMA of this M-tile runs while its softmax reads or writes TMEM
+        // the softmax has loaded S(lt): S(lt+1) may go into the buffer now,
+        // unless this tile's P residual is parked there
+        wait_ok(s_free + mi, (uint32_t)jt & 1u);
+        if (!exact && lt + 1 < lt1) {
+          acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
+          issue_s(mi, (it + 1) % NS);
+        }
         wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
         issue_pv(mi, b, st, lt == lt0, exact);
-        wait_ok(o_done + mi, (uint32_t)jt & 1u);
-        tc_fence_after();
-        if (lane == 0) mbar_arrive(empty + st);  // this M-tile is done with the K/V stage
-        if (lt + 1 < lt1) {
+        if (exact && lt + 1 < lt1) {
+          wait_ok(o_done + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+          tc_fence_after();
           acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
-          issue_s(mi, b ^ 1, (it + 1) % NS);
+          issue_s(mi, (it + 1) % NS);
         }
+        __syncwarp();
       }
     }
     // drain: every MMA the issuers started has finished before TMEM is released
@@ -286,8 +301,9 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 
     for (int lt = lt0; lt < lt1; ++lt, ++jt) {
       const int b = jt & 1;
-      const uint32_t tS = tmem + lane_bits + 256 + 64 * (2 * mi + b);
-      wait_ok(s_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+      const uint32_t tS = tmem + lane_bits + 256 + 64 * mi;
+      const uint32_t tP = tmem + lane_bits + 384 + 64 * mi + 32 * b;
+      wait_ok(s_full + mi, (uint32_t)jt & 1u);
       tc_fence_after();
       float sv[64];
       {
@@ -301,6 +317,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(u[j]);
       }
+      tc_fence_before();
+      mbar_arrive(s_free + mi);  // the S buffer may take the next tile's scores
       const int k0 = lt * kTK;
       const bool masked = k0 + kTK > g.n_prefix;
       if (masked) {
@@ -329,7 +347,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         // move the reference max only when it grew by more than 2^8 (exact either way)
         const bool need = (m_new - m_used) * cl2 > 8.f;
         if (__any_sync(0xffffffffu, need)) {
-          wait_ok(o_done + mi, (uint32_t)(jt - 1) & 1u);  // O holds every PV up to the previous tile
+          wait_ok(o_done + 2 * mi + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);  // O holds every PV up to tile jt-1
           tc_fence_after();
           const float alpha = need ? exp2f((m_used - m_new) * cl2) : 1.f;
 #pragma unroll
@@ -351,8 +369,11 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
       uint32_t ph[32];
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short add chains
+      // the P buffer of this parity is free once the PV of tile jt-2 is done
+      // (every PV completion is waited for in order, two tiles late)
       if (masked) {
-        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts)
+        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts,
+        // parked in the S buffer, which the issuer refills only after that PV)
         uint32_t pl[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -361,8 +382,10 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           ls4[j & 3] += a + bq;
           split_bf16x2(a, bq, ph[j], pl[j]);
         }
-        tmem_st32(tS, ph);
-        tmem_st32(tS + 32, pl);
+        if (jt >= 2) wait_ok(o_done + 2 * mi + b, (uint32_t)((jt - 2) >> 1) & 1u);
+        tc_fence_after();
+        tmem_st32(tP, ph);
+        tmem_st32(tS, pl);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -371,7 +394,9 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           ls4[j & 3] += a + bq;
           ph[j] = pack_bf16(a, bq);
         }
-        tmem_st32(tS, ph);
+        if (jt >= 2) wait_ok(o_done + 2 * mi + b, (uint32_t)((jt - 2) >> 1) & 1u);
+        tc_fence_after();
+        tmem_st32(tP, ph);
       }
       const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l += ls;
@@ -380,8 +405,9 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       mbar_arrive(p_full + 2 * mi + b);
     }
 
-    // ---- epilogue: O / l for this segment part ----
-    wait_ok(o_done + mi, (uint32_t)(jt - 1) & 1u);
+    // ---- epilogue: O / l for this segment part (the last two PVs, in order) ----
+    if (jt >= 2) wait_ok(o_done + 2 * mi + (jt & 1), (uint32_t)((jt - 2) >> 1) & 1u);
+    wait_ok(o_done + 2 * mi + ((jt - 1) & 1), (uint32_t)((jt - 1) >> 1) & 1u);
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_nat = l > 0.f ? (m_used * cl2 + log2f(l)) * kLn2 : -INFINITY;
