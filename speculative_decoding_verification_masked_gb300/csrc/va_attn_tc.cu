@@ -8,25 +8,23 @@
 //
 // Roles (11 warps when the segment has two 128-row M-tiles):
 //   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
-//                    = one TMEM lane.  Loads S from TMEM and releases the S
-//                    buffer at once, applies the draft bitmask, runs the online
-//                    softmax, writes P (bf16) into one of two P buffers,
-//                    rescales O in TMEM when the row max grows by more than
-//                    2^8, and writes the output row.
+//                    = one TMEM lane.  Reads S from TMEM, applies the draft
+//                    bitmask, runs the online softmax, writes P (bf16; on
+//                    draft tiles also the bf16 residual) back over S, rescales
+//                    O in TMEM when the row max grows by more than 2^8, and
+//                    writes the output row.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
 //                    sparse) into a 4-stage ring (shared with the other kernel)
 //   warps 4*NMT+1+i  MMA issuer of M-tile i: S_i = Q_i K^T (M128 N64 K128, both
-//                    operands in shared memory, K-major 128B swizzle) into the
-//                    M-tile's S buffer as soon as the softmax has loaded the
-//                    previous S, and O_i += P_i V (A = P from TMEM, B = V as an
-//                    MN-major operand).  P never shares columns with S, so an
-//                    S MMA never overwrites what a running PV MMA reads (MMAs
-//                    with different accumulators are not ordered); only on a
-//                    draft tile, whose bf16 residual of P is parked in the S
-//                    buffer, does the next S wait for the PV.  Issuer 0 owns
-//                    the TMEM allocation.
-// TMEM (512 columns): O_i at 128*i, S_i at 256 + 64*i, P_i[b] at
-// 384 + 64*i + 32*b (bf16 pairs).
+//                    operands in shared memory, K-major 128B swizzle) into one
+//                    of two S/P buffers, and O_i += P_i V (A = P from TMEM, B =
+//                    V as an MN-major operand).  S of tile t+2 goes into the
+//                    buffer of tile t once PV(t), which reads P from it, has
+//                    completed (MMAs with different accumulators are not
+//                    ordered against each other), so it is computed while the
+//                    softmax works on tile t+1.  Issuer 0 owns the TMEM
+//                    allocation.
+// TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
 // Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
 // barrier sequence of all roles intact, drains and frees TMEM.
 #include <cuda.h>
@@ -50,8 +48,8 @@ struct TcSmem {
   static constexpr int kStageBytes = StageGeom<__nv_bfloat16, 128>::kStageBytes;
   static constexpr int kStagesOff = kQBytes;
   static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
-  // barriers: full[4], empty[4], s_full[2], s_free[2], p_full[2][2], o_done[2][2], drain
-  static constexpr int kNumBars = 2 * kTcStages + 2 + 2 + 4 + 4 + 1;
+  // barriers: full[4], empty[4], s_full[2][2], p_full[2][2], o_done[2][2], drain
+  static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kTstartOff = kMiscOff + 16;
   static constexpr int kThreads = (5 * NMT + 1) * 32;
@@ -82,9 +80,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::kBarOff);
   uint64_t *full = bars;
   uint64_t *empty = bars + NS;
-  uint64_t *s_full = bars + 2 * NS;       // [i]
-  uint64_t *s_free = bars + 2 * NS + 2;   // [i]: the softmax has loaded S_i
-  uint64_t *p_full = bars + 2 * NS + 4;   // [i][b] at 2*i + b, b = tile parity
+  uint64_t *s_full = bars + 2 * NS;       // [i][b] at 2*i + b, b = tile parity = buffer
+  uint64_t *p_full = bars + 2 * NS + 4;   // [i][b]
   uint64_t *o_done = bars + 2 * NS + 8;   // [i][b]
   uint64_t *drain = bars + 2 * NS + 12;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
@@ -97,18 +94,13 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   const int lane = tid & 31;
   const int c = blockIdx.x;
 
-  pdl_launch_dependents();
-
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, use_tma ? 1 : 32);
       mbar_init(empty + i, NMT);  // one arrive per M-tile issuer
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(s_free + i, 128);
-    }
     for (int i = 0; i < 4; ++i) {
+      mbar_init(s_full + i, 1);
       mbar_init(p_full + i, 128);
       mbar_init(o_done + i, 1);
     }
@@ -117,12 +109,18 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     fence_mbar_init();
   }
   const CtaRange cr = plan_cta(p, tstart);  // contains __syncthreads
-  if (c >= cr.G) return;
+  if (c >= cr.G) {
+    pdl_launch_dependents();
+    return;
+  }
   const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
 
   if (warp == kProducerWarp) {
     bool pok = true;
     produce_tiles<__nv_bfloat16, D, NS>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag, use_tma, pok);
+    // the merge grid may become resident once the last tiles are on their way
+    // (it waits for this grid's completion before reading anything)
+    pdl_launch_dependents();
     return;
   }
 
@@ -168,32 +166,37 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_s = [&](int i, int st) {  // S_i = Q_i K^T
+    // Shared-memory descriptors are built once; a K-step or stage offset is an
+    // add to the start-address field (addresses stay below 256 KB, so the
+    // 14-bit field never carries).
+    const uint64_t dQ = umma_sdesc(smem_u32(sQ) + mi * 32768, 16, 1024);
+    const uint64_t dK0 = umma_sdesc(smem_u32(stages), 16, 1024);
+    const uint64_t dV0 = umma_sdesc(smem_u32(stages) + Geo::kTileBytes, 8192, 1024);
+    constexpr uint64_t kStageStep = Geo::kStageBytes >> 4;
+    auto issue_s = [&](int i, int b, int st) {  // S_i(b) = Q_i K^T
       if (!ok || lane != 0) return;
       tc_fence_after();
-      const uint32_t q0 = smem_u32(sQ) + i * 32768;
-      const uint32_t k0 = smem_u32(stages + st * Geo::kStageBytes);
-      const uint32_t dS = tmem + 256 + 64 * i;
+      const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
+      const uint32_t dS = tmem + 256 + 64 * (2 * i + b);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const uint64_t a = umma_sdesc(q0 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-        const uint64_t bb = umma_sdesc(k0 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-        umma_ss(dS, a, bb, id_s, ks > 0);
+        const uint64_t qoff = (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
+        const uint64_t koff = (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
+        umma_ss(dS, dQ + qoff, dK + koff, id_s, ks > 0 ? 1u : 0u);
       }
-      umma_commit(s_full + i);
+      umma_commit(s_full + 2 * i + b);
     };
     auto issue_pv = [&](int i, int b, int st, bool first, bool exact) {  // O_i += P_i V
       if (!ok || lane != 0) return;
       tc_fence_after();
-      const uint32_t v0 = smem_u32(stages + st * Geo::kStageBytes + Geo::kTileBytes);
-      const uint32_t aP = tmem + 384 + 64 * i + 32 * b;
-      const uint32_t aL = tmem + 256 + 64 * i;  // bf16 residual of P (draft tiles) in the S buffer
+      const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
+      const uint32_t aP = tmem + 256 + 64 * (2 * i + b);  // P hi; the residual 32 columns on
       const uint32_t dO = tmem + 128 * i;
 #pragma unroll
       for (int kk = 0; kk < kTK / 16; ++kk) {
-        const uint64_t bb = umma_sdesc(v0 + kk * 2048, 8192, 1024);
+        const uint64_t bb = dV + (uint64_t)((kk * 2048) >> 4);
         umma_ts(dO, aP + kk * 8, bb, id_o, (!first || kk > 0) ? 1u : 0u);
-        if (exact) umma_ts(dO, aL + kk * 8, bb, id_o, 1u);
+        if (exact) umma_ts(dO, aP + 32 + kk * 8, bb, id_o, 1u);
       }
       umma_commit(o_done + 2 * i + b);
       umma_commit(empty + st);  // this M-tile is done with the K/V stage once these complete
@@ -204,26 +207,26 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const int lt0 = max(tstart[s], t0) - tstart[s];
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoftThreads + kMmaThreads);  // Q of this segment is in shared memory
+      // S of the first two tiles (both buffers are free: the previous
+      // segment's PVs completed before its epilogue)
       acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
-      issue_s(mi, it % NS);
+      issue_s(mi, jt & 1, it % NS);
+      if (lt0 + 1 < lt1) {
+        acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt0 + 1, g);
+        issue_s(mi, (jt + 1) & 1, (it + 1) % NS);
+      }
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int st = it % NS;
         const int b = jt & 1;
         const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
-        // the softmax has loaded S(lt): S(lt+1) may go into the buffer now,
-        // unless this tile's P residual is parked there
-        wait_ok(s_free + mi, (uint32_t)jt & 1u);
-        if (!exact && lt + 1 < lt1) {
-          acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
-          issue_s(mi, (it + 1) % NS);
-        }
         wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
         issue_pv(mi, b, st, lt == lt0, exact);
-        if (exact && lt + 1 < lt1) {
+        if (lt + 2 < lt1) {
+          // S(t+2) into this buffer once PV(t) has read P from it
           wait_ok(o_done + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
           tc_fence_after();
-          acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt + 1, g);
-          issue_s(mi, (it + 1) % NS);
+          acquire_stage((it + 2) % NS, (uint32_t)((it + 2) / NS) & 1u, lt + 2, g);
+          issue_s(mi, b, (it + 2) % NS);
         }
         __syncwarp();
       }
@@ -301,9 +304,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 
     for (int lt = lt0; lt < lt1; ++lt, ++jt) {
       const int b = jt & 1;
-      const uint32_t tS = tmem + lane_bits + 256 + 64 * mi;
-      const uint32_t tP = tmem + lane_bits + 384 + 64 * mi + 32 * b;
-      wait_ok(s_full + mi, (uint32_t)jt & 1u);
+      const uint32_t tS = tmem + lane_bits + 256 + 64 * (2 * mi + b);
+      wait_ok(s_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
       tc_fence_after();
       float sv[64];
       {
@@ -317,8 +319,6 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(u[j]);
       }
-      tc_fence_before();
-      mbar_arrive(s_free + mi);  // the S buffer may take the next tile's scores
       const int k0 = lt * kTK;
       const bool masked = k0 + kTK > g.n_prefix;
       if (masked) {
@@ -369,11 +369,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
       uint32_t ph[32];
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short add chains
-      // the P buffer of this parity is free once the PV of tile jt-2 is done
-      // (every PV completion is waited for in order, two tiles late)
       if (masked) {
-        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts,
-        // parked in the S buffer, which the issuer refills only after that PV)
+        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts)
         uint32_t pl[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -382,10 +379,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           ls4[j & 3] += a + bq;
           split_bf16x2(a, bq, ph[j], pl[j]);
         }
-        if (jt >= 2) wait_ok(o_done + 2 * mi + b, (uint32_t)((jt - 2) >> 1) & 1u);
-        tc_fence_after();
-        tmem_st32(tP, ph);
-        tmem_st32(tS, pl);
+        tmem_st32(tS, ph);
+        tmem_st32(tS + 32, pl);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -394,9 +389,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           ls4[j & 3] += a + bq;
           ph[j] = pack_bf16(a, bq);
         }
-        if (jt >= 2) wait_ok(o_done + 2 * mi + b, (uint32_t)((jt - 2) >> 1) & 1u);
-        tc_fence_after();
-        tmem_st32(tP, ph);
+        tmem_st32(tS, ph);
       }
       const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l += ls;
