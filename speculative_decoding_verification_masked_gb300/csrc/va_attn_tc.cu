@@ -15,15 +15,16 @@
 //                    writes the output row.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
 //                    sparse) into a 4-stage ring (shared with the other kernel)
-//   warps 4*NMT+1+i  MMA issuer of M-tile i: S_i = Q_i K^T (M128 N64 K128, both
-//                    operands in shared memory, K-major 128B swizzle) into one
-//                    of two S/P buffers, and O_i += P_i V (A = P from TMEM, B =
-//                    V as an MN-major operand).  S of tile t+2 goes into the
-//                    buffer of tile t once PV(t), which reads P from it, has
-//                    completed (MMAs with different accumulators are not
-//                    ordered against each other), so it is computed while the
-//                    softmax works on tile t+1.  Issuer 0 owns the TMEM
+//   warps 4*NMT+1+i  PV issuer of M-tile i: O_i += P_i V (A = P from TMEM, B =
+//                    V as an MN-major operand).  Issuer 0 owns the TMEM
 //                    allocation.
+//   warp 5*NMT+1     S issuer of every M-tile: S_i = Q_i K^T (M128 N64 K128,
+//                    both operands in shared memory, K-major 128B swizzle)
+//                    into one of two S/P buffers per M-tile.  S of tile t goes
+//                    into the buffer of tile t-2 once PV(t-2), which reads P
+//                    from it, has completed (MMAs with different accumulators
+//                    are not ordered against each other); with S and PV on
+//                    separate warps neither waits behind the other's issue.
 // TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
 // Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
 // barrier sequence of all roles intact, drains and frees TMEM.
@@ -52,7 +53,7 @@ struct TcSmem {
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kTstartOff = kMiscOff + 16;
-  static constexpr int kThreads = (5 * NMT + 1) * 32;
+  static constexpr int kThreads = (5 * NMT + 2) * 32;
 };
 
 // Offset of chunk c (16 B) of row r in a 128-row, 128B-swizzled Q tile pair.
@@ -70,8 +71,9 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   constexpr int NS = kTcStages;
   constexpr int kSoftThreads = 128 * NMT;
   constexpr int kProducerWarp = 4 * NMT;
-  constexpr int kMmaWarp0 = 4 * NMT + 1;  // issuer of M-tile i is warp kMmaWarp0 + i
-  constexpr int kMmaThreads = 32 * NMT;
+  constexpr int kMmaWarp0 = 4 * NMT + 1;  // PV issuer of M-tile i is warp kMmaWarp0 + i
+  constexpr int kSWarp = 5 * NMT + 1;     // S issuer of every M-tile
+  constexpr int kMmaThreads = 32 * (NMT + 1);
   constexpr int kBarQ = 1, kBarSoft = 2, kBarEnd = 3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       mbar_init(p_full + i, 128);
       mbar_init(o_done + i, 1);
     }
-    mbar_init(drain, NMT);
+    mbar_init(drain, NMT + 1);  // one commit per MMA-issuing warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -138,8 +140,9 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   const int group = p.Hq / p.Hkv;
 
   if (warp >= kMmaWarp0) {
-    // =========================== MMA issuer of M-tile mi ===========================
-    const int mi = warp - kMmaWarp0;
+    // ================== MMA issuers: PV of M-tile mi, or S of all ==================
+    const bool s_issuer = warp == kSWarp;
+    const int mi = s_issuer ? 0 : warp - kMmaWarp0;
     const uint32_t id_s = umma_idesc(128, 64, 0, 0);
     const uint32_t id_o = umma_idesc(128, 128, 0, 1);
     int it = 0, jt = 0;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     // Shared-memory descriptors are built once; a K-step or stage offset is an
     // add to the start-address field (addresses stay below 256 KB, so the
     // 14-bit field never carries).
-    const uint64_t dQ = umma_sdesc(smem_u32(sQ) + mi * 32768, 16, 1024);
+    const uint64_t dQ0 = umma_sdesc(smem_u32(sQ), 16, 1024);
     const uint64_t dK0 = umma_sdesc(smem_u32(stages), 16, 1024);
     const uint64_t dV0 = umma_sdesc(smem_u32(stages) + Geo::kTileBytes, 8192, 1024);
     constexpr uint64_t kStageStep = Geo::kStageBytes >> 4;
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t qoff = (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
         const uint64_t koff = (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
-        umma_ss(dS, dQ + qoff, dK + koff, id_s, ks > 0 ? 1u : 0u);
+        umma_ss(dS, dQ0 + (uint64_t)(i * (32768 >> 4)) + qoff, dK + koff, id_s, ks > 0 ? 1u : 0u);
       }
       umma_commit(s_full + 2 * i + b);
     };
@@ -207,26 +210,22 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       const int lt0 = max(tstart[s], t0) - tstart[s];
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoftThreads + kMmaThreads);  // Q of this segment is in shared memory
-      // S of the first two tiles (both buffers are free: the previous
-      // segment's PVs completed before its epilogue)
-      acquire_stage(it % NS, (uint32_t)(it / NS) & 1u, lt0, g);
-      issue_s(mi, jt & 1, it % NS);
-      if (lt0 + 1 < lt1) {
-        acquire_stage((it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u, lt0 + 1, g);
-        issue_s(mi, (jt + 1) & 1, (it + 1) % NS);
-      }
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int st = it % NS;
         const int b = jt & 1;
-        const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
-        wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
-        issue_pv(mi, b, st, lt == lt0, exact);
-        if (lt + 2 < lt1) {
-          // S(t+2) into this buffer once PV(t) has read P from it
-          wait_ok(o_done + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
-          tc_fence_after();
-          acquire_stage((it + 2) % NS, (uint32_t)((it + 2) / NS) & 1u, lt + 2, g);
-          issue_s(mi, b, (it + 2) % NS);
+        if (s_issuer) {
+          // S(t) of each M-tile into buffer b once PV(t-2) has read P from it
+          for (int i = 0; i < NMT; ++i) {
+            if (jt >= 2) wait_ok(o_done + 2 * i + b, (uint32_t)((jt - 2) >> 1) & 1u);
+            if (i == 0) wait_ok(full + st, (uint32_t)(it / NS) & 1u);
+            tc_fence_after();
+            issue_s(i, b, st);
+          }
+        } else {
+          const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
+          wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+          acquire_stage(st, (uint32_t)(it / NS) & 1u, lt, g);
+          issue_pv(mi, b, st, lt == lt0, exact);
         }
         __syncwarp();
       }
@@ -237,7 +236,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     tc_fence_before();
     named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);
     tc_fence_after();
-    if (mi == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    if (warp == kMmaWarp0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
     return;
   }
 

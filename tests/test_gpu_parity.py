@@ -166,6 +166,22 @@ def test_paged_small(page_size):
     _check(wt, "parent")
 
 
+@pytest.mark.parametrize("layout", ["paged", "sparse"])
+def test_many_rows_through_gathers(layout):
+    """More than 64 packed rows (rows on the TMEM lanes) with K/V rows gathered
+    through a page table or a verify set, ragged lengths, a token tree."""
+    if layout == "paged":
+        w = W.make_workload("paged", seed=41, B=3, L_lo=100, L_hi=700, page_size=16, T=32, tree="depth", depth=5)
+        _check(w, "parent")
+    else:
+        w = W.make_workload("sparse", seed=42, B=2, L_lo=300, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60,
+                            T=24, tree="depth", depth=4)
+        ref = oracle.verify(w)
+        out, lse = run_library(w, "parent", indices=dev_i32(ref["indices"]), n_indices=dev_i32(ref["n_indices"]))
+        torch.cuda.synchronize()
+        compare(out, lse, ref)
+
+
 def test_sparse_small_with_library_indices():
     w = W.make_workload("sparse", seed=3, B=3, L_lo=200, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60)
     ref = oracle.verify(w)
