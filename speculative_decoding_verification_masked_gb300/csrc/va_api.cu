@@ -71,15 +71,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D map over a dense cache [rows = B * len][Hkv][D]: boxes of 64 tokens x
-// one kv-head x 128 bytes of the head dimension, 128-byte swizzled.
-bool encode_cache_map(CUtensorMap *m, const void *base, va_dtype dt, int D, int Hkv, long long rows) {
+// 3-D map over a cache of rows [rows][Hkv][D] (dense: rows = B * len; paged:
+// rows = num_pages * page_size): boxes of box_rows tokens x one kv-head x 128
+// bytes of the head dimension, 128-byte swizzled.
+bool encode_cache_map(CUtensorMap *m, const void *base, va_dtype dt, int D, int Hkv, long long rows, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint32_t es = dt == VA_DTYPE_BF16 ? 2 : 4;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
-  const cuuint32_t box[3] = {128 / es, 1, 64};
+  const cuuint32_t box[3] = {128 / es, 1, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, dt == VA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -271,8 +272,19 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   if (layout == VA_LAYOUT_DENSE) {
     const long long rows = (long long)s.B * len_cap;
     if (rows >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "B * max_cache_len must be below 2^31");
-    if (!encode_cache_map(&tmk, k, s.dtype, s.D, s.Hkv, rows) || !encode_cache_map(&tmv, v, s.dtype, s.D, s.Hkv, rows))
+    if (!encode_cache_map(&tmk, k, s.dtype, s.D, s.Hkv, rows, 64) ||
+        !encode_cache_map(&tmv, v, s.dtype, s.D, s.Hkv, rows, 64))
       return fail(VA_ERR_CUDA, "could not encode the TMA tensor maps of the cache");
+    p.tma_box = 64;
+  } else if (layout == VA_LAYOUT_PAGED && page_size >= 8) {
+    // one TMA box per page (at most 64 rows): a box lands on whole 1024-byte
+    // swizzle atoms of the stage.  Smaller pages, or a pool the map cannot
+    // describe, are gathered with cp.async instead.
+    const long long rows = (long long)num_pages * page_size;
+    const int box = page_size < 64 ? page_size : 64;
+    if (rows < (1ll << 31) && encode_cache_map(&tmk, k, s.dtype, s.D, s.Hkv, rows, box) &&
+        encode_cache_map(&tmv, v, s.dtype, s.D, s.Hkv, rows, box))
+      p.tma_box = box;
   }
   cudaError_t e = va::launch_attention(p, tmk, tmv, grid < 1 ? 1 : grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
   uint64_t *empty = full + NS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NS);
   int *tstart = reinterpret_cast<int *>(empty + NS) + 4;
-  const bool use_tma = p.layout == VA_LAYOUT_DENSE;
+  const bool use_tma = p.tma_box > 0;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
-  const bool use_tma = p.layout == VA_LAYOUT_DENSE;
+  const bool use_tma = p.tma_box > 0;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;

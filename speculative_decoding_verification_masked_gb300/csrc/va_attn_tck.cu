@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   float4 *red = reinterpret_cast<float4 *>(smem + SM::kRedOff);
   float *row_inv = reinterpret_cast<float *>(smem + SM::kRowInvOff);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
-  const bool use_tma = p.layout == VA_LAYOUT_DENSE;
+  const bool use_tma = p.tma_box > 0;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;

@@ -28,6 +28,8 @@ struct AttnParams {
   const void *q, *k, *v;
   int len_cap;  // dense/sparse: max_cache_len; paged: max_pages * page_size
   int num_pages, page_shift, max_pages;
+  int tma_box;  // rows of one TMA box of the cache (dense 64; paged: the page size, at
+                // most 64); 0 = rows gathered with 16-byte cp.async (sparse, pages below 8 rows)
   const int32_t *page_table;
   const int32_t *seqlens;
   const int32_t *indices, *n_indices;

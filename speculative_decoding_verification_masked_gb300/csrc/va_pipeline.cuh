@@ -296,7 +296,6 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
                                              uint64_t *full, uint64_t *empty, volatile int *abort_flag,
                                              bool use_tma, bool &ok) {
   using C = StageGeom<Tin, D, TK>;
-  constexpr int kBox = 64;          // rows of one TMA box
   constexpr int kRowSets = TK / 32; // key rows per lane in the gather
   const int lane = threadIdx.x & 31;
   const uint64_t policy = l2_evict_first_policy();
@@ -333,24 +332,42 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
       uint8_t *vdst = kdst + C::kTileBytes;
       const int k0 = lt * TK;
       if (use_tma) {
-        // dense: TK consecutive tokens of this kv-head, boxes of 64 rows per
-        // 128-byte column; rows past the segment end arrive too (other tokens
-        // or zero fill) and are masked
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full + st, (uint32_t)C::kStageBytes);
-          const int row0 = g.b * p.len_cap + k0;
+        // TMA boxes of BR rows x one kv-head x 128 bytes of the head dimension.
+        // Dense: BR = 64 consecutive tokens; rows past the segment end arrive
+        // too (other tokens or zero fill) and are masked.  Paged: one box per
+        // page (BR = page size, at most 64), so a box never crosses a page;
+        // boxes that start past the segment end are not loaded (their page
+        // entries need not exist) and the rows they would fill are masked.
+        const int BR = p.tma_box;
+        const int nbox = TK / BR;  // boxes per 128-byte column (at most 16)
+        const bool paged = p.layout == VA_LAYOUT_PAGED;
+        const int nb = paged ? min(nbox, (g.nkeys - k0 + BR - 1) / BR) : nbox;
+        if (lane == 0) mbar_arrive_expect_tx(full + st, (uint32_t)(nb * BR * 128 * C::kHalves * 2));
+        __syncwarp();
+        if (lane < nb) {
+          const int slot = k0 + lane * BR;
+          int row;
+          if (paged) {
+            int page = __ldg(p.page_table + (size_t)g.b * p.max_pages + (slot >> p.page_shift));
+            if (page < 0 || page >= p.num_pages) {
+              record_status(p.status, VA_ERR_DEVICE_BOUNDS);
+              page = 0;
+            }
+            row = (page << p.page_shift) + (slot & ((1 << p.page_shift) - 1));
+          } else {
+            row = g.b * p.len_cap + slot;
+          }
+          const int off = lane * BR * 128;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
-#pragma unroll
-            for (int rb = 0; rb < TK / kBox; ++rb) {
-              const int off = h * TK * 128 + rb * kBox * 128;
-              tma_load_3d(kdst + off, tmk, h * (128 / (int)sizeof(Tin)), g.hkv, row0 + rb * kBox, full + st, policy);
-              tma_load_3d(vdst + off, tmv, h * (128 / (int)sizeof(Tin)), g.hkv, row0 + rb * kBox, full + st, policy);
-            }
+            tma_load_3d(kdst + h * TK * 128 + off, tmk, h * (128 / (int)sizeof(Tin)), g.hkv, row, full + st, policy);
+            tma_load_3d(vdst + h * TK * 128 + off, tmv, h * (128 / (int)sizeof(Tin)), g.hkv, row, full + st, policy);
           }
         }
       } else {
-        // paged / sparse: gather rows with 16-byte copies; rows past the end are zero-filled
+        // paged (pages below 8 rows) / sparse: gather rows with 16-byte
+        // copies, rows past the end zero-filled.  Lane l resolves rows l + 32j;
+        // a pass copies RPP rows, each row's address shuffled from its lane.
         const Tin *rows[kRowSets];
 #pragma unroll
         for (int j = 0; j < kRowSets; ++j)
@@ -358,20 +375,21 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
         constexpr int CPR = C::kChunks;  // lanes per row
         constexpr int RPP = 32 / CPR;    // rows per pass
         const int cc = lane % CPR;
-#pragma unroll 4
-        for (int i = 0; i < TK / RPP; ++i) {
-          const int r = i * RPP + lane / CPR;
-          uint64_t a = 0;
+        const int rsub = lane / CPR;
+        const int nvalid = g.nkeys - k0;
 #pragma unroll
-          for (int j = 0; j < kRowSets; ++j) {
-            const uint64_t x = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(rows[j]), r & 31);
-            if ((r >> 5) == j) a = x;
+        for (int j = 0; j < kRowSets; ++j) {
+#pragma unroll
+          for (int i = 0; i < 32 / RPP; ++i) {
+            const int rl = i * RPP + rsub;
+            const uintptr_t a = (uintptr_t)__shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(rows[j]), rl);
+            const int r = 32 * j + rl;
+            const uintptr_t src = a + (uintptr_t)cc * 16u;
+            const uint32_t n = r < nvalid ? 16u : 0u;
+            const uint32_t off = swz<TK>(r, cc);
+            cp_async_16(kdst + off, reinterpret_cast<const void *>(src), n);
+            cp_async_16(vdst + off, reinterpret_cast<const void *>(src + vdelta), n);
           }
-          const uintptr_t src = (uintptr_t)a + (uintptr_t)cc * 16u;
-          const uint32_t n = (k0 + r < g.nkeys) ? 16u : 0u;
-          const uint32_t off = swz<TK>(r, cc);
-          cp_async_16(kdst + off, reinterpret_cast<const void *>(src), n);
-          cp_async_16(vdst + off, reinterpret_cast<const void *>(src + vdelta), n);
         }
         cp_async_mbar_arrive(full + st);
       }

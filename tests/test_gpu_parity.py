@@ -154,8 +154,10 @@ def test_random_masks_and_empty_rows():
     assert torch.all(out[0, 5] == 0)
 
 
-@pytest.mark.parametrize("page_size", [1, 16, 64])
+@pytest.mark.parametrize("page_size", [1, 4, 8, 16, 64, 128])
 def test_paged_small(page_size):
+    """Pages below 8 rows are gathered with cp.async; larger ones arrive as
+    one TMA box per page (128-row pages as two 64-row boxes)."""
     w = W.make_workload("paged", seed=page_size, B=5, L_lo=3, L_hi=700, page_size=page_size, spare_pages=7)
     _check(w, "mask")
     wb = W.make_workload("paged", seed=page_size + 1, B=4, L_lo=40, L_hi=300, page_size=page_size,
@@ -164,6 +166,49 @@ def test_paged_small(page_size):
     wt = W.make_workload("paged", seed=page_size + 2, B=3, L_lo=40, L_hi=300, page_size=page_size,
                          tree="depth", T=16, depth=4)
     _check(wt, "parent")
+
+
+@pytest.mark.parametrize("page_size", [4, 8, 32])
+def test_paged_fp32(page_size):
+    """fp32 pages (mma.sync kernel): 128-byte boxes hold 32 values."""
+    w = W.make_workload("tiny", seed=60 + page_size, layout="paged", B=3, L_lo=5, L_hi=400,
+                        page_size=page_size, spare_pages=3)
+    eo, el, _ = _check(w, "mask")
+    assert eo < 1e-4 and el < 1e-4
+
+
+def _poison_unread_rows(w):
+    """NaN in every cache row no sequence reads: the tail of each sequence's
+    last page, spare pages, dense rows past L + T.  Tiles that load whole
+    boxes bring such rows into shared memory; they must not reach the output."""
+    nan = torch.tensor(float("nan"), dtype=w.q.dtype)
+    if w.layout == "paged":
+        read = np.zeros(w.k_pages.shape[:2], dtype=bool)
+        for b in range(w.B):
+            n = int(w.seqlens[b]) + w.T
+            for slot in range(n):
+                read[w.page_table[b, slot // w.page_size], slot % w.page_size] = True
+        m = torch.from_numpy(~read)
+        w.k_pages[m] = nan
+        w.v_pages[m] = nan
+    else:
+        for b in range(w.B):
+            n = int(w.seqlens[b]) + w.T
+            w.k_cache[b, n:] = nan
+            w.v_cache[b, n:] = nan
+    return w
+
+
+@pytest.mark.parametrize("case", ["paged8", "paged16", "paged128", "dense", "dense_tree"])
+def test_unread_cache_rows_poisoned(case):
+    if case.startswith("paged"):
+        ps = int(case[5:])
+        w = W.make_workload("paged", seed=70 + ps, B=4, L_lo=30, L_hi=500, page_size=ps, spare_pages=5)
+    elif case == "dense":
+        w = W.make_workload("chain", seed=71, B=3, L_lo=30, L_hi=700, extra_slots=150)
+    else:
+        w = W.make_workload("tree", seed=72, B=2, Hkv=2, L_lo=30, L_hi=700, extra_slots=150)
+    _check(_poison_unread_rows(w), "mask")
 
 
 @pytest.mark.parametrize("layout", ["paged", "sparse"])
