@@ -46,7 +46,15 @@ namespace va {
 
 constexpr int kTkKeys = 128;  // keys per tile
 constexpr int kTkStages = 3;
-constexpr int kTkThreads = 192;
+// Warps: 0-3 softmax, 4 producer, 5 MMA issuer, then NR <= 32 adds a second
+// producer warp that shares the cp.async gather of the paged / sparse layouts
+// (one warp's gather is limited by the copies it can keep in flight).  Seven
+// warps leave at most two per SM sub-partition, so 255 registers stay available.
+template <int NR>
+struct TkCfg {
+  static constexpr int kProducers = NR <= 32 ? 2 : 1;
+  static constexpr int kThreads = (5 + kProducers) * 32;
+};
 
 template <int NR>
 struct TkSmem {
@@ -253,7 +261,7 @@ __device__ __forceinline__ void merge_rows_warp(const AttnParams &p, int s, int 
 }
 
 template <int NR>
-__global__ void __launch_bounds__(kTkThreads, 1)
+__global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
     verify_attn_tck_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv) {
   using SM = TkSmem<NR>;
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full + i, use_tma ? 1 : 32);
+      mbar_init(full + i, use_tma ? 1 : 32 * TkCfg<NR>::kProducers);
       mbar_init(empty + i, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -309,10 +317,11 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   if (c >= cr.G) return;
   const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp > kMmaWarp) {
     bool pok = true;
-    produce_tiles<__nv_bfloat16, D, NS, TK, 2>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag,
-                                               use_tma, pok);
+    produce_tiles<__nv_bfloat16, D, NS, TK, 2, TkCfg<NR>::kProducers>(
+        p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag, use_tma, pok,
+        warp == kProducerWarp ? 0 : warp - kMmaWarp);
     return;
   }
 
@@ -786,7 +795,7 @@ static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, con
   // cooperative: every CTA is resident, so the wait for a segment's parts ends
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kTkThreads);
+  cfg.blockDim = dim3(TkCfg<NR>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

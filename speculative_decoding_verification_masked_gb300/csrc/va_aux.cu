@@ -52,6 +52,7 @@ constexpr int kIdxThreads = 1024;
 constexpr int kIdxMaxL = 131072;
 constexpr int kIdxBitmapWords = kIdxMaxL / 32 + 4;
 constexpr int kIdxCacheKeys = 36864;  // keys held in shared memory when L fits
+constexpr int kIdxLoads = 16;         // score loads in flight per thread while caching
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -112,7 +113,20 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
   const bool cached = L <= kIdxCacheKeys;
   auto excluded = [&](int i) -> bool { return (sm.bitmap[i >> 5] >> (i & 31)) & 1u; };
   if (cached) {
-    for (int i = tid; i < L; i += kIdxThreads) sm.keys[i] = excluded(i) ? 0u : order_key(__ldg(src + i));
+    // kIdxLoads independent loads in flight per thread, then the conversions
+    for (int base = 0; base < L; base += kIdxThreads * kIdxLoads) {
+      float v[kIdxLoads];
+#pragma unroll
+      for (int u = 0; u < kIdxLoads; ++u) {
+        const int i = base + u * kIdxThreads + tid;
+        v[u] = i < L ? __ldg(src + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kIdxLoads; ++u) {
+        const int i = base + u * kIdxThreads + tid;
+        if (i < L) sm.keys[i] = excluded(i) ? 0u : order_key(v[u]);
+      }
+    }
     __syncthreads();
   }
   auto key_at = [&](int i) -> uint32_t {
@@ -240,6 +254,15 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
     record_status(p.status, VA_ERR_DEVICE_BOUNDS);
     L = L < 0 ? 0 : cap;
   }
+  const size_t row = ((size_t)b * p.Hkv + h);
+  {
+    // both score rows are read in full below: start bringing them into L2 now
+    const float *sd = p.sd + row * p.stride, *st = p.st + row * p.stride;
+    for (int j = tid; 32 * j < L; j += kIdxThreads) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(sd + 32 * j));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(st + 32 * j));
+    }
+  }
   const int nwords = (L + 31) / 32;
   // fixed part: sinks [0, a) and window [wlo, L)
   const int a = min(p.n_sink, L);
@@ -256,7 +279,6 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   const int fixed = a + (L - wlo) - max(0, a - wlo);
   const int room = max(0, p.budget - fixed);
   const int ncand = L - fixed;
-  const size_t row = ((size_t)b * p.Hkv + h);
   const int m1 = max(0, min(min(p.m_draft, room), ncand));
   select_top(p.sd + row * p.stride, L, m1, sm);
   const int m2 = max(0, min(room - m1, ncand - m1));

@@ -290,14 +290,19 @@ __device__ __forceinline__ CtaRange plan_cta(const AttnParams &p, int *tstart) {
 // once tile j - MAXF has landed, and with a cap the second tile waits for the
 // first, so at the start of the kernel the first tile of every CTA does not
 // share the memory system with the rest of the ring.
-template <typename Tin, int D, int NS, int TK = kTK, int MAXF = NS>
+//
+// NPW warps may share the gather (warp pw takes the row sets j = pw mod NPW,
+// and full[] then counts 32 * NPW arrivals); only warp 0 issues TMA boxes.
+template <typename Tin, int D, int NS, int TK = kTK, int MAXF = NS, int NPW = 1>
 __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                              const int *tstart, const CtaRange &cr, uint8_t *stages,
                                              uint64_t *full, uint64_t *empty, volatile int *abort_flag,
-                                             bool use_tma, bool &ok) {
+                                             bool use_tma, bool &ok, int pw = 0) {
   using C = StageGeom<Tin, D, TK>;
   constexpr int kRowSets = TK / 32; // key rows per lane in the gather
+  static_assert(kRowSets % NPW == 0, "row sets split evenly over the producer warps");
   const int lane = threadIdx.x & 31;
+  if (use_tma && pw != 0) return 0;
   const uint64_t policy = l2_evict_first_policy();
   const Tin *kbase = static_cast<const Tin *>(p.k);
   const uintptr_t vdelta = reinterpret_cast<uintptr_t>(p.v) - reinterpret_cast<uintptr_t>(p.k);
@@ -305,6 +310,20 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
     prefetch_tmap(tmk);
     prefetch_tmap(tmv);
   }
+  // gather: the row addresses of the tile being issued; those of the next
+  // tile are loaded before this tile's copies are issued, so their latency
+  // hides behind the copies
+  const Tin *rows[kRowSets];
+  auto load_rows = [&](const Seg &gg, int ltt, const Tin **dst) {
+#pragma unroll
+    for (int j = 0; j < kRowSets; ++j) {
+      if (j % NPW != pw) continue;
+      const int k = ltt * TK + lane + 32 * j;
+      dst[j] = k < gg.nkeys ? key_row<Tin, D>(p, gg, k, kbase) : kbase;
+    }
+  };
+  if (!use_tma && cr.s0 < p.S && tstart[cr.s0] < cr.t1)
+    load_rows(seg_info(p, cr.s0, false), max(tstart[cr.s0], cr.t0) - tstart[cr.s0], rows);
   int it = 0;
   for (int s = cr.s0; s < p.S && tstart[s] < cr.t1; ++s) {
     const Seg g = seg_info(p, s, false);
@@ -368,10 +387,15 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
         // paged (pages below 8 rows) / sparse: gather rows with 16-byte
         // copies, rows past the end zero-filled.  Lane l resolves rows l + 32j;
         // a pass copies RPP rows, each row's address shuffled from its lane.
-        const Tin *rows[kRowSets];
-#pragma unroll
-        for (int j = 0; j < kRowSets; ++j)
-          rows[j] = (k0 + lane + 32 * j < g.nkeys) ? key_row<Tin, D>(p, g, k0 + lane + 32 * j, kbase) : kbase;
+        const Tin *nrows[kRowSets];
+        bool has_next = true;
+        if (lt + 1 < lt1) {
+          load_rows(g, lt + 1, nrows);
+        } else if (s + 1 < p.S && tstart[s + 1] < cr.t1) {
+          load_rows(seg_info(p, s + 1, false), max(tstart[s + 1], cr.t0) - tstart[s + 1], nrows);
+        } else {
+          has_next = false;
+        }
         constexpr int CPR = C::kChunks;  // lanes per row
         constexpr int RPP = 32 / CPR;    // rows per pass
         const int cc = lane % CPR;
@@ -379,6 +403,7 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
         const int nvalid = g.nkeys - k0;
 #pragma unroll
         for (int j = 0; j < kRowSets; ++j) {
+          if (j % NPW != pw) continue;
 #pragma unroll
           for (int i = 0; i < 32 / RPP; ++i) {
             const int rl = i * RPP + rsub;
@@ -392,6 +417,10 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
           }
         }
         cp_async_mbar_arrive(full + st);
+        if (has_next) {
+#pragma unroll
+          for (int j = 0; j < kRowSets; ++j) rows[j] = nrows[j];
+        }
       }
     }
   }
