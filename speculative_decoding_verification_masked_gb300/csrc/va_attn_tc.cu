@@ -61,7 +61,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int NMT>
+template <int NMT, bool kTma>
 __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     verify_attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
-  const bool use_tma = p.tma_box > 0;
+  constexpr bool use_tma = kTma;  // tiles by TMA boxes (dense, paged), else cp.async gathers
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 
   if (warp == kProducerWarp) {
     bool pok = true;
-    produce_tiles<__nv_bfloat16, D, NS>(p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag, use_tma, pok);
+    produce_tiles<__nv_bfloat16, D, NS, kTK, NS, 1, kTma ? 1 : 0>(p, &tmk, &tmv, tstart, cr, stages, full, empty,
+                                                                  abort_flag, use_tma, pok);
     // the merge grid may become resident once the last tiles are on their way
     // (it waits for this grid's completion before reading anything)
     pdl_launch_dependents();
@@ -454,11 +455,11 @@ size_t attn_tc_smem_required(const AttnParams &p) {
   return p.rows_pad > 128 ? tc_smem_bytes<2>(p.S) : tc_smem_bytes<1>(p.S);
 }
 
-template <int NMT>
+template <int NMT, bool kTma>
 static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                cudaStream_t stream) {
   const size_t smem = tc_smem_bytes<NMT>(p.S);
-  auto kern = verify_attn_tc_kernel<NMT>;
+  auto kern = verify_attn_tc_kernel<NMT, kTma>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, TcSmem<NMT>::kThreads, smem, stream>>>(p, tmk, tmv);
@@ -467,7 +468,10 @@ static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, cons
 
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream) {
-  return p.rows_pad > 128 ? launch_tc_t<2>(p, tmk, tmv, grid, stream) : launch_tc_t<1>(p, tmk, tmv, grid, stream);
+  const bool tma = p.tma_box > 0;
+  if (p.rows_pad > 128)
+    return tma ? launch_tc_t<2, true>(p, tmk, tmv, grid, stream) : launch_tc_t<2, false>(p, tmk, tmv, grid, stream);
+  return tma ? launch_tc_t<1, true>(p, tmk, tmv, grid, stream) : launch_tc_t<1, false>(p, tmk, tmv, grid, stream);
 }
 
 }  // namespace va

@@ -50,9 +50,9 @@ constexpr int kTkStages = 3;
 // producer warp that shares the cp.async gather of the paged / sparse layouts
 // (one warp's gather is limited by the copies it can keep in flight).  Seven
 // warps leave at most two per SM sub-partition, so 255 registers stay available.
-template <int NR>
+template <int NR, bool kTma>
 struct TkCfg {
-  static constexpr int kProducers = NR <= 32 ? 2 : 1;
+  static constexpr int kProducers = !kTma && NR <= 32 ? 2 : 1;
   static constexpr int kThreads = (5 + kProducers) * 32;
 };
 
@@ -99,6 +99,30 @@ struct WarpScatterMax {
     } else {
       v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
       WarpScatterMax<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+// The same reduce-scatter with sums: lane l ends with the warp's sum of the
+// rows WarpScatterMax leaves it.
+template <int N, int O>
+struct WarpScatterSum {
+  static __device__ __forceinline__ void run(float *v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (N >= 2) {
+      constexpr int H = N / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      WarpScatterSum<H, O / 2>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      WarpScatterSum<1, O / 2>::run(v, lane);
     }
   }
 };
@@ -260,8 +284,8 @@ __device__ __forceinline__ void merge_rows_warp(const AttnParams &p, int s, int 
   }
 }
 
-template <int NR>
-__global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
+template <int NR, bool kTma>
+__global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     verify_attn_tck_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv) {
   using SM = TkSmem<NR>;
@@ -271,6 +295,9 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
   constexpr int NS = kTkStages;
   constexpr int NC = SM::kNC;
   constexpr int kSoft = 128;
+  // NR <= 32: the row sums l are kept by the softmax threads (each over its own
+  // keys, reduced once per segment part) instead of a ones-operand MMA per tile
+  constexpr bool kRegL = NR <= 32;
   constexpr int kProducerWarp = 4, kMmaWarp = 5;
   constexpr int kBarQ = 1, kBarRed = 2, kBarSoft = 3, kBarEnd = 4;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -291,7 +318,7 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
   float4 *red = reinterpret_cast<float4 *>(smem + SM::kRedOff);
   float *row_inv = reinterpret_cast<float *>(smem + SM::kRowInvOff);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
-  const bool use_tma = p.tma_box > 0;
+  constexpr bool use_tma = kTma;  // tiles by TMA boxes (dense, paged), else cp.async gathers
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -300,7 +327,7 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full + i, use_tma ? 1 : 32 * TkCfg<NR>::kProducers);
+      mbar_init(full + i, use_tma ? 1 : 32 * TkCfg<NR, kTma>::kProducers);
       mbar_init(empty + i, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -319,7 +346,7 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
 
   if (warp == kProducerWarp || warp > kMmaWarp) {
     bool pok = true;
-    produce_tiles<__nv_bfloat16, D, NS, TK, 2, TkCfg<NR>::kProducers>(
+    produce_tiles<__nv_bfloat16, D, NS, TK, 2, TkCfg<NR, kTma>::kProducers, kTma ? 1 : 0>(
         p, &tmk, &tmv, tstart, cr, stages, full, empty, abort_flag, use_tma, pok,
         warp == kProducerWarp ? 0 : warp - kMmaWarp);
     return;
@@ -387,7 +414,7 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
         const uint64_t off = (uint64_t)((kk * 2048) >> 4);
         const uint32_t acc = kk > 0 ? 1u : acc0;
         umma_ss(tO, dV + off, dP + off, id_o, acc);
-        umma_ts(tL, tOnes, dP + off, id_l, acc);
+        if constexpr (!kRegL) umma_ts(tL, tOnes, dP + off, id_l, acc);
       }
       if (exact) {  // the bf16 residual of P on draft tiles
         constexpr uint64_t lo = (uint64_t)((TK * 128) >> 4);
@@ -395,7 +422,7 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
         for (int kk = 0; kk < TK / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk * 2048) >> 4);
           umma_ss(tO, dV + off, dP + lo + off, id_o, 1u);
-          umma_ts(tL, tOnes, dP + lo + off, id_l, 1u);
+          if constexpr (!kRegL) umma_ts(tL, tOnes, dP + lo + off, id_l, 1u);
         }
       }
       umma_commit(o_done + b);
@@ -485,6 +512,10 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
     float mu[NR];  // reference max per row, log2 units
 #pragma unroll
     for (int r = 0; r < NR; ++r) mu[r] = -INFINITY;
+    // (kRegL) sums over this thread's keys of the bf16 P the PV MMAs multiply
+    float lsum[kRegL ? NR : 1];
+#pragma unroll
+    for (int r = 0; r < (kRegL ? NR : 1); ++r) lsum[r] = 0.f;
 
     for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
       const int b = jt & 1;
@@ -571,11 +602,15 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
           alpha[r] = mu[r] == -INFINITY ? 0.f : ex2_approx(mu[r] - mnew);
           mu[r] = mnew;
         }
+        if constexpr (kRegL) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) lsum[r] *= alpha[r];
+        }
         if (lt != lt0) {
           wait_ok(o_done + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);  // O and l hold every PV up to tile jt-1
           tc_fence_after();
           tmem_scale_cols<NR>(tO, x);
-          tmem_scale_cols<NR>(tL, x);
+          if constexpr (!kRegL) tmem_scale_cols<NR>(tL, x);
           tmem_st_wait();
         }
         load_scores();
@@ -594,6 +629,10 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
             const float a = ex2_approx(fmaf(x[r], cl2, mu[r] == -INFINITY ? 0.f : -mu[r]));
             const float bq = ex2_approx(fmaf(x[r + 1], cl2, mu[r + 1] == -INFINITY ? 0.f : -mu[r + 1]));
             split_bf16x2(a, bq, h[q], l[q]);
+            if constexpr (kRegL) {  // exactly the bf16 hi + lo the MMAs multiply
+              lsum[r] += __uint_as_float(h[q] << 16) + __uint_as_float(l[q] << 16);
+              lsum[r + 1] += __uint_as_float(h[q] & 0xFFFF0000u) + __uint_as_float(l[q] & 0xFFFF0000u);
+            }
           }
           const int off = tid * 128 + ((cc ^ sw) << 4);
           *reinterpret_cast<uint4 *>(pk + off) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -615,6 +654,10 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
           for (int q = 0; q < 4; ++q) {
             const int r = 8 * cc + 2 * q;
             h[q] = pack_bf16(ex2_approx(fmaf(x[r], cl2, -mu[r])), ex2_approx(fmaf(x[r + 1], cl2, -mu[r + 1])));
+            if constexpr (kRegL) {
+              lsum[r] += __uint_as_float(h[q] << 16);
+              lsum[r + 1] += __uint_as_float(h[q] & 0xFFFF0000u);
+            }
           }
           *reinterpret_cast<uint4 *>(pk + tid * 128 + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
@@ -634,14 +677,28 @@ __global__ void __launch_bounds__(TkCfg<NR>::kThreads, 1)
     // lane); its l and reference max are picked out of the register arrays by
     // predicated selects, so the rows are done by the threads in parallel
     float my_l = 0.f, my_mu = 0.f;
+    if constexpr (kRegL) {
+      // l: this thread's key sums, reduce-scattered over the warp (lane l gets
+      // row l, or l / 2 for 16 rows), then the four warps' sums of each row
+      WarpScatterSum<NR, 16>::run(lsum, lane);
+      if ((lane & (32 / NR - 1)) == 0) reinterpret_cast<float *>(red)[(lane / (32 / NR)) * 4 + warp] = lsum[0];
+      named_bar_sync(kBarSoft, kSoft);
+      if (tid < NR) {
+        const float4 l4 = red[tid];
+        my_l = (l4.x + l4.y) + (l4.z + l4.w);
+      }
 #pragma unroll
-    for (int h = 0; h < NR / CH; ++h) {
-      float lv[CH];
-      tmem_ld_f<CH>(tL + h * CH, lv);
+      for (int j = 0; j < NR; ++j) my_mu = tid == j ? mu[j] : my_mu;
+    } else {
 #pragma unroll
-      for (int j = 0; j < CH; ++j) {
-        my_l = tid == h * CH + j ? lv[j] : my_l;
-        my_mu = tid == h * CH + j ? mu[h * CH + j] : my_mu;
+      for (int h = 0; h < NR / CH; ++h) {
+        float lv[CH];
+        tmem_ld_f<CH>(tL + h * CH, lv);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          my_l = tid == h * CH + j ? lv[j] : my_l;
+          my_mu = tid == h * CH + j ? mu[h * CH + j] : my_mu;
+        }
       }
     }
     if (tid < p.R) {
@@ -785,17 +842,17 @@ size_t attn_tck_smem_required(const AttnParams &p) {
                                                                        : tck_smem_bytes<64>(p.S);
 }
 
-template <int NR>
+template <int NR, bool kTma>
 static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream) {
   const size_t smem = tck_smem_bytes<NR>(p.S);
-  auto kern = verify_attn_tck_kernel<NR>;
+  auto kern = verify_attn_tck_kernel<NR, kTma>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // cooperative: every CTA is resident, so the wait for a segment's parts ends
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(TkCfg<NR>::kThreads);
+  cfg.blockDim = dim3(TkCfg<NR, kTma>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -808,9 +865,12 @@ static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, con
 
 cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream) {
-  if (p.rows_pad <= 16) return launch_tck_t<16>(p, tmk, tmv, grid, stream);
-  if (p.rows_pad <= 32) return launch_tck_t<32>(p, tmk, tmv, grid, stream);
-  return launch_tck_t<64>(p, tmk, tmv, grid, stream);
+  const bool tma = p.tma_box > 0;
+  if (p.rows_pad <= 16)
+    return tma ? launch_tck_t<16, true>(p, tmk, tmv, grid, stream) : launch_tck_t<16, false>(p, tmk, tmv, grid, stream);
+  if (p.rows_pad <= 32)
+    return tma ? launch_tck_t<32, true>(p, tmk, tmv, grid, stream) : launch_tck_t<32, false>(p, tmk, tmv, grid, stream);
+  return tma ? launch_tck_t<64, true>(p, tmk, tmv, grid, stream) : launch_tck_t<64, false>(p, tmk, tmv, grid, stream);
 }
 
 }  // namespace va

@@ -45,14 +45,16 @@ cudaError_t launch_tree_mask(int B, int T, const int32_t *parent, uint32_t *mask
 // One CTA per (sequence, kv-head).  The chosen set lives in a bitmap over
 // positions, so the output comes out sorted by a prefix count over bitmap
 // words.  Each top-k is an exact radix select on order-preserving 32-bit keys
-// (four 8-bit digits, most significant first); keys equal to the threshold are
-// taken in increasing position order, which is the tie rule.
+// (digits of 11, 11 and 10 bits, most significant first); keys equal to the
+// threshold are taken in increasing position order, which is the tie rule.
 // ---------------------------------------------------------------------------
 constexpr int kIdxThreads = 1024;
 constexpr int kIdxMaxL = 131072;
 constexpr int kIdxBitmapWords = kIdxMaxL / 32 + 4;
 constexpr int kIdxCacheKeys = 36864;  // keys held in shared memory when L fits
 constexpr int kIdxLoads = 16;         // score loads in flight per thread while caching
+constexpr int kIdxBins = 2048;        // bins of one radix digit (11 bits)
+constexpr int kIdxCopies = 8;         // histogram copies, each shared by 4 warps
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -62,7 +64,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 struct IdxSmem {
   uint32_t *bitmap;
-  uint32_t *hist;
+  uint32_t *hist;  // kIdxCopies histograms of kIdxBins bins
   int *scratch;
   uint32_t *keys;
 };
@@ -97,23 +99,82 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int &to
   return res;
 }
 
-// Select the k largest keys among positions [0, L) not yet in the bitmap and
-// add them to it.  k must not exceed the number of such positions.
+// Keys still to be added to the chosen set: every key k != 0 with
+// (k & pmask) >= prefix.  A select whose threshold bucket is taken whole
+// leaves this pending; the next fill of the key cache (or the final pass)
+// applies it while it reads the old keys.
+struct Take {
+  uint32_t prefix, pmask;
+  bool active;
+};
+
+__device__ __forceinline__ bool take_key(uint32_t key, const Take &t) {
+  return t.active && key != 0u && (key & t.pmask) >= t.prefix;
+}
+
+// Digits of the radix select: bits 31-21, 20-10 and 9-0.  Eleven bits in the
+// first digit already split the exponent and the top mantissa bits, so
+// continuous scores are usually resolved after two digits.
+__device__ __forceinline__ int digit_shift(int d) { return d == 0 ? 21 : d == 1 ? 10 : 0; }
+__device__ __forceinline__ int digit_bits(int d) { return d == 2 ? 10 : 11; }
+
+__device__ __forceinline__ void hist_zero(const IdxSmem &sm) {
+  for (int j = threadIdx.x; j < kIdxCopies * kIdxBins; j += kIdxThreads) sm.hist[j] = 0;
+}
+
+// The bucket of digit d that holds the kk-th largest counted key: thread t
+// owns the 1 or 2 bins just below bin 2047 - per * t (bins scanned from the
+// top).  Sets scratch[64] = bin, [65] = rank inside it, [66] = bucket taken whole.
+__device__ __forceinline__ void find_bucket(int d, int kk, const IdxSmem &sm) {
+  const int nb = 1 << digit_bits(d);
+  const int per = nb / kIdxThreads;  // 2 or 1
+  const int tid = threadIdx.x;
+  int c[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (j < per) {
+      const int bin = nb - 1 - (tid * per + j);
+#pragma unroll
+      for (int h = 0; h < kIdxCopies; ++h) c[j] += (int)sm.hist[h * kIdxBins + bin];
+    }
+  }
+  int tot;
+  int run = block_exclusive_scan(c[0] + c[1], sm.scratch, tot);
+  if (run < kk && kk <= run + c[0] + c[1]) {
+    for (int j = 0; j < per; ++j) {
+      if (run + c[j] >= kk) {
+        sm.scratch[64] = nb - 1 - (tid * per + j);
+        sm.scratch[65] = kk - run;
+        sm.scratch[66] = (run + c[j] == kk) ? 1 : 0;
+        break;
+      }
+      run += c[j];
+    }
+  }
+  __syncthreads();
+}
+
+// Select the k largest keys among positions [0, L) not yet in the bitmap (nor
+// in `prev`, still pending) and return them as a pending Take -- or add them
+// to the bitmap now when the key cache is not used or ties decide.
+// k must not exceed the number of such positions.
 //
-// Radix select, most significant digit first.  After each 8-bit digit the
-// bucket holding the k-th largest key is known together with how many keys
-// above it are already certain.  If that bucket holds exactly the keys still
-// needed, every key at or above it is taken and the search stops (the usual
-// case for continuous scores).  Otherwise the search narrows to the bucket; if
-// keys equal to the final threshold still outnumber the quota, they are taken
-// in increasing position order (the tie rule).
-__device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
-  if (k <= 0) return;
+// Radix select, most significant digit first.  After each digit the bucket
+// holding the k-th largest key is known together with how many keys above it
+// are already certain.  If that bucket holds exactly the keys still needed,
+// every key at or above it is taken.  Otherwise the search narrows to the
+// bucket; if keys equal to the final threshold still outnumber the quota,
+// they are taken in increasing position order (the tie rule).
+__device__ Take select_top(const float *src, int L, int k, const IdxSmem &sm, const Take prev) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t *myhist = sm.hist + kIdxBins * (warp % kIdxCopies);
   const bool cached = L <= kIdxCacheKeys;
   auto excluded = [&](int i) -> bool { return (sm.bitmap[i >> 5] >> (i & 31)) & 1u; };
+  hist_zero(sm);
+  __syncthreads();
   if (cached) {
-    // kIdxLoads independent loads in flight per thread, then the conversions
+    // fill the key cache, kIdxLoads loads in flight per thread; apply the
+    // pending take of the previous select; histogram of the first digit
     for (int base = 0; base < L; base += kIdxThreads * kIdxLoads) {
       float v[kIdxLoads];
 #pragma unroll
@@ -124,11 +185,28 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
 #pragma unroll
       for (int u = 0; u < kIdxLoads; ++u) {
         const int i = base + u * kIdxThreads + tid;
-        if (i < L) sm.keys[i] = excluded(i) ? 0u : order_key(v[u]);
+        if (base + u * kIdxThreads >= L) break;  // uniform over the block
+        bool ex = false, took = false;
+        if (i < L) {
+          took = take_key(sm.keys[i], prev);
+          ex = took || excluded(i);
+        }
+        const uint32_t word = __ballot_sync(0xffffffffu, took);
+        if (lane == 0 && word != 0u) sm.bitmap[((base + u * kIdxThreads) >> 5) + warp] |= word;
+        if (i < L) {
+          const uint32_t key = ex ? 0u : order_key(v[u]);
+          sm.keys[i] = key;
+          if (key != 0u) atomicAdd(myhist + (key >> 21), 1u);
+        }
       }
     }
-    __syncthreads();
+  } else {
+    for (int i = tid; i < L; i += kIdxThreads) {
+      if (!excluded(i)) atomicAdd(myhist + (order_key(__ldg(src + i)) >> 21), 1u);
+    }
   }
+  __syncthreads();
+  if (k <= 0) return Take{0u, 0u, false};
   auto key_at = [&](int i) -> uint32_t {
     if (cached) return sm.keys[i];
     return excluded(i) ? 0u : order_key(__ldg(src + i));
@@ -136,79 +214,44 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
 
   uint32_t prefix = 0, pmask = 0;
   int kk = k;
-  int shift = 24;
   bool exact_bucket = false;
-  for (; shift >= 0; shift -= 8) {
-    // per-warp private histograms (hist + 256 * warp), then summed per bin
-    for (int j = tid; j < 32 * 256; j += kIdxThreads) sm.hist[j] = 0;
-    __syncthreads();
-    uint32_t *myhist = sm.hist + 256 * warp;
-    for (int base = 0; base < L; base += kIdxThreads) {
-      const int i = base + tid;
-      if (i < L) {
-        const uint32_t key = key_at(i);
-        if (key != 0u && (key & pmask) == prefix) atomicAdd(myhist + ((key >> shift) & 255u), 1u);
-      }
-    }
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t tot = 0;
-#pragma unroll 8
-      for (int w = 0; w < 32; ++w) tot += sm.hist[256 * w + tid];
-      sm.hist[tid] = tot;  // bin totals in the first 256 entries (warp 0's copy, already read)
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255-8l .. 248-8l, scanned from the top
-      int c[8];
-      int sum = 0;
+  for (int d = 0; d < 3; ++d) {
+    const int shift = digit_shift(d), bits = digit_bits(d);
+    if (d > 0) {
+      hist_zero(sm);
+      __syncthreads();
+      for (int base = 0; base < L; base += kIdxThreads * 4) {
+        uint32_t kv[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = (int)sm.hist[255 - 8 * lane - j];
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - sum;
-      if (run < kk && kk <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run + c[j] >= kk) {
-            sm.scratch[64] = 255 - 8 * lane - j;
-            sm.scratch[65] = kk - run;
-            sm.scratch[66] = (run + c[j] == kk) ? 1 : 0;  // the bucket is taken whole
-            break;
-          }
-          run += c[j];
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * kIdxThreads + tid;
+          kv[u] = i < L ? key_at(i) : 0u;
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (kv[u] != 0u && (kv[u] & pmask) == prefix) atomicAdd(myhist + ((kv[u] >> shift) & ((1u << bits) - 1u)), 1u);
       }
+      __syncthreads();
     }
-    __syncthreads();
+    find_bucket(d, kk, sm);
     prefix |= (uint32_t)sm.scratch[64] << shift;
-    pmask |= 255u << shift;
+    pmask |= ((1u << bits) - 1u) << shift;
     kk = sm.scratch[65];
     exact_bucket = sm.scratch[66] != 0;
     __syncthreads();
     if (exact_bucket) break;
   }
   if (exact_bucket) {
-    // every key whose digits down to `shift` are >= the chosen prefix is taken
+    const Take t{prefix, pmask, true};
+    if (cached) return t;  // applied by the next pass over the key cache
     for (int base = 0; base < L; base += kIdxThreads) {
       const int i = base + tid;
-      bool take = false;
-      if (i < L) {
-        const uint32_t key = key_at(i);
-        take = key != 0u && (key & pmask) >= prefix;
-      }
+      const bool take = i < L && take_key(key_at(i), t);
       const uint32_t word = __ballot_sync(0xffffffffu, take);
       if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
     }
     __syncthreads();
-    return;
+    return Take{0u, 0u, false};
   }
   // ties at the full 32-bit threshold exceed the quota: above-threshold keys plus
   // the first kk equal keys in position order
@@ -227,6 +270,7 @@ __device__ void select_top(const float *src, int L, int k, const IdxSmem &sm) {
     taken_eq += tot;
   }
   __syncthreads();
+  return Take{0u, 0u, false};
 }
 
 struct IndexParams {
@@ -243,7 +287,7 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   IdxSmem sm;
   sm.bitmap = ism;
   sm.hist = ism + kIdxBitmapWords;
-  sm.scratch = reinterpret_cast<int *>(sm.hist + 32 * 256);
+  sm.scratch = reinterpret_cast<int *>(sm.hist + kIdxCopies * kIdxBins);
   sm.keys = reinterpret_cast<uint32_t *>(sm.scratch + 128);
   const int tid = threadIdx.x;
   const int b = blockIdx.x / p.Hkv;
@@ -280,9 +324,21 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   const int room = max(0, p.budget - fixed);
   const int ncand = L - fixed;
   const int m1 = max(0, min(min(p.m_draft, room), ncand));
-  select_top(p.sd + row * p.stride, L, m1, sm);
   const int m2 = max(0, min(room - m1, ncand - m1));
-  select_top(p.st + row * p.stride, L, m2, sm);
+  const Take none{0u, 0u, false};
+  Take t = m1 > 0 ? select_top(p.sd + row * p.stride, L, m1, sm, none) : none;
+  if (m2 > 0) t = select_top(p.st + row * p.stride, L, m2, sm, t);
+  if (t.active) {
+    // the last pending take, from the key cache
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int base = 0; base < L; base += kIdxThreads) {
+      const int i = base + tid;
+      const bool take = i < L && take_key(sm.keys[i], t);
+      const uint32_t word = __ballot_sync(0xffffffffu, take);
+      if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
+    }
+    __syncthreads();
+  }
 
   // bitmap -> ascending positions
   int32_t *out = p.indices + row * p.budget;
@@ -307,7 +363,7 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
 }
 
 size_t build_index_smem_bytes() {
-  return sizeof(uint32_t) * (kIdxBitmapWords + 32 * 256 + 128 + kIdxCacheKeys);
+  return sizeof(uint32_t) * (kIdxBitmapWords + kIdxCopies * kIdxBins + 128 + kIdxCacheKeys);
 }
 
 cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,

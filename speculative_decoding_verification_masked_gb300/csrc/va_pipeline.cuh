@@ -293,7 +293,11 @@ __device__ __forceinline__ CtaRange plan_cta(const AttnParams &p, int *tstart) {
 //
 // NPW warps may share the gather (warp pw takes the row sets j = pw mod NPW,
 // and full[] then counts 32 * NPW arrivals); only warp 0 issues TMA boxes.
-template <typename Tin, int D, int NS, int TK = kTK, int MAXF = NS, int NPW = 1>
+// PATH fixes the way tiles arrive at compile time (1 = TMA boxes only, 0 =
+// cp.async gather only; -1 = chosen by use_tma): a kernel built for one way
+// carries none of the other's code, which measurably slows the warps that
+// share the kernel.
+template <typename Tin, int D, int NS, int TK = kTK, int MAXF = NS, int NPW = 1, int PATH = -1>
 __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                              const int *tstart, const CtaRange &cr, uint8_t *stages,
                                              uint64_t *full, uint64_t *empty, volatile int *abort_flag,
@@ -302,6 +306,7 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
   constexpr int kRowSets = TK / 32; // key rows per lane in the gather
   static_assert(kRowSets % NPW == 0, "row sets split evenly over the producer warps");
   const int lane = threadIdx.x & 31;
+  if constexpr (PATH >= 0) use_tma = PATH == 1;
   if (use_tma && pw != 0) return 0;
   const uint64_t policy = l2_evict_first_policy();
   const Tin *kbase = static_cast<const Tin *>(p.k);

@@ -278,6 +278,38 @@ def test_build_index_bit_exact(L_lo, L_hi):
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
 
 
+@pytest.mark.parametrize("dist", ["normal", "negative", "wide", "few_distinct", "step"])
+@pytest.mark.parametrize("m_draft", [0, 300])
+def test_build_index_score_distributions(dist, m_draft):
+    """Score shapes that move the k-th key across the radix digits: signed and
+    negative scores, a wide exponent range, a handful of distinct values (ties
+    at every digit), and values spaced so bucket edges fall at the threshold."""
+    rng = np.random.default_rng(hash((dist, m_draft)) % 2**32)
+    B, Hkv = 3, 2
+    seqlens = rng.integers(9000, 30000, size=B).astype(np.int32)
+    stride = int(seqlens.max())
+
+    def draw():
+        if dist == "normal":
+            return rng.standard_normal((B, Hkv, stride))
+        if dist == "negative":
+            return -rng.random((B, Hkv, stride)) - 1.0
+        if dist == "wide":
+            return rng.standard_normal((B, Hkv, stride)) * np.exp2(rng.integers(-60, 60, size=(B, Hkv, stride)))
+        if dist == "few_distinct":
+            return rng.integers(0, 7, size=(B, Hkv, stride)) * 0.25
+        # step: consecutive float32 values, so digits differ only in the low bits
+        return np.float32(1.0) + rng.integers(0, 4096, size=(B, Hkv, stride)) * np.float32(2.0 ** -23)
+
+    sd = draw().astype(np.float32)
+    st = draw().astype(np.float32)
+    args = (4, 200, m_draft, 1500)
+    ref_idx, ref_n = oracle.build_verify_index(sd, st, seqlens, *args)
+    idx, n = va.verify_build_index(dev_i32(seqlens), torch.from_numpy(sd).cuda(), torch.from_numpy(st).cuda(), *args)
+    assert np.array_equal(n.cpu().numpy(), ref_n)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
 # ----------------------------------------------------------------------------
 # combine (exposed merge)
 # ----------------------------------------------------------------------------
