@@ -322,6 +322,105 @@ def build_verify_index(score_draft, score_target, seqlens, n_sink, window, m_dra
 
 
 # ----------------------------------------------------------------------------
+# after verification: greedy acceptance over the tree, and the KV commit
+# (Dustin section 1, step 5: accepted tokens join the cache, rejected ones are
+# dropped; HiSpec section 2: the entries of rejected tokens are removed before
+# the next phase, and the output equals the target model's own decoding)
+# ----------------------------------------------------------------------------
+
+def greedy_accept(parent, draft_tokens, target_next):
+    """Greedy acceptance over token trees.
+
+    Reading (the pages fix the guarantee, not the tree rule): a draft node is
+    accepted when its parent is accepted -- or it hangs off the committed
+    prefix (parent -1) -- and its token equals the target model's greedy
+    token after that parent.  The committed path is the accepted root path of
+    greatest depth, the one ending at the smallest node index when several
+    are equally deep; the bonus token is the target's greedy token after the
+    path's last node (after the prefix when nothing is accepted).
+
+    parent [B][T] int32 with -1 <= parent[t] < t; draft_tokens [B][T] int32;
+    target_next [B][T+1] int32: column 0 is the target's greedy next token
+    after the committed prefix, column t+1 the one after draft node t.
+    Returns path [B][T] int32 (node indices from the root down, tail -1),
+    n_accept [B] int32 and bonus [B] int32.
+    """
+    parent = np.asarray(parent)
+    draft = np.asarray(draft_tokens)
+    tgt = np.asarray(target_next)
+    B, T = parent.shape
+    path = np.full((B, T), -1, dtype=np.int32)
+    n_acc = np.zeros(B, dtype=np.int32)
+    bonus = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        accepted = [False] * T
+        depth = [0] * T
+        for t in range(T):  # a parent comes before its children
+            p = int(parent[b, t])
+            if not -1 <= p < t:
+                raise ValueError("parent[%d][%d] = %d is not an earlier node" % (b, t, p))
+            up = p < 0 or accepted[p]
+            accepted[t] = up and int(draft[b, t]) == int(tgt[b, p + 1])
+            depth[t] = 1 if p < 0 else depth[p] + 1
+        best = -1
+        for t in range(T):
+            if accepted[t] and (best < 0 or depth[t] > depth[best]):
+                best = t
+        if best < 0:
+            bonus[b] = tgt[b, 0]
+            continue
+        nodes = []
+        t = best
+        while t >= 0:
+            nodes.append(t)
+            t = int(parent[b, t])
+        nodes.reverse()
+        path[b, : len(nodes)] = nodes
+        n_acc[b] = len(nodes)
+        bonus[b] = tgt[b, best + 1]
+    return path, n_acc, bonus
+
+
+def commit_kv_dense(k_cache, v_cache, seqlens, path, n_accept):
+    """KV commit after acceptance, contiguous cache [B][len][Hkv][D].
+
+    The draft rows of sequence b sit at slots L_b .. L_b+T-1 (L_b =
+    seqlens[b]).  For j < n_accept[b] the row at slot L_b + path[b][j] is
+    moved to slot L_b + j, in every kv-head of both caches; every other slot
+    keeps its content.  Rows are copied, not computed (any element type).
+    Returns new k, v and seqlens + n_accept.
+    """
+    k = np.array(k_cache, copy=True)
+    v = np.array(v_cache, copy=True)
+    for b in range(len(seqlens)):
+        L = int(seqlens[b])
+        a = int(n_accept[b])
+        src = [L + int(path[b][j]) for j in range(a)]
+        k[b, L:L + a] = np.asarray(k_cache)[b, src]
+        v[b, L:L + a] = np.asarray(v_cache)[b, src]
+    return k, v, (np.asarray(seqlens) + np.asarray(n_accept)).astype(np.int32)
+
+
+def commit_kv_paged(k_pages, v_pages, page_table, page_size, seqlens, path, n_accept):
+    """The same commit over a paged pool [P][page][Hkv][D]: logical slot s of
+    sequence b is row s % page_size of page page_table[b][s // page_size]."""
+    k = np.array(k_pages, copy=True)
+    v = np.array(v_pages, copy=True)
+
+    def where(b, slot):
+        return int(page_table[b][slot // page_size]), slot % page_size
+
+    for b in range(len(seqlens)):
+        L = int(seqlens[b])
+        for j in range(int(n_accept[b])):
+            sp, sr = where(b, L + int(path[b][j]))
+            dp, dr = where(b, L + j)
+            k[dp, dr] = np.asarray(k_pages)[sp, sr]
+            v[dp, dr] = np.asarray(v_pages)[sp, sr]
+    return k, v, (np.asarray(seqlens) + np.asarray(n_accept)).astype(np.int32)
+
+
+# ----------------------------------------------------------------------------
 # whole verification step for a workload object (duck-typed)
 # ----------------------------------------------------------------------------
 

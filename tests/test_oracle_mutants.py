@@ -93,3 +93,53 @@ def test_pristine_oracle_passes_the_pins(tmp_path):
 def test_planted_mistake_is_caught(tmp_path, name):
     with oracle.swapped_library(_build_variant(tmp_path, name, MUTANTS[name])):
         assert not _pins_pass(), f"pins did not catch mutant {name}"
+
+
+# ----------------------------------------------------------------------------
+# the Python-side oracle functions (greedy acceptance, KV commit): the planted
+# mistake is applied to the function's source and the function swapped in
+# ----------------------------------------------------------------------------
+
+PY_MUTANTS = {
+    "accept_ignores_parent": ("greedy_accept", "up = p < 0 or accepted[p]", "up = True"),
+    "accept_target_column": ("greedy_accept", "int(tgt[b, p + 1])", "int(tgt[b, p])"),
+    "accept_ties_to_larger_end": ("greedy_accept", "depth[t] > depth[best]", "depth[t] >= depth[best]"),
+    "accept_bonus_column": ("greedy_accept", "bonus[b] = tgt[b, best + 1]", "bonus[b] = tgt[b, best]"),
+    "commit_no_move": ("commit_kv_dense", "src = [L + int(path[b][j]) for j in range(a)]",
+                       "src = [L + j for j in range(a)]"),
+    "commit_paged_row": ("commit_kv_paged", "return int(page_table[b][slot // page_size]), slot % page_size",
+                         "return int(page_table[b][slot // page_size]), (slot + 1) % page_size"),
+}
+
+
+def _py_pins_pass():
+    from tests import test_oracle_pins as pins
+    try:
+        pins.test_greedy_accept_hand()
+        for seed in range(12):
+            pins.test_greedy_accept_brute_force(seed)
+        pins.test_greedy_accept_chain_is_prefix_match()
+        pins.test_commit_kv_hand()
+        pins.test_commit_kv_paged_equals_dense()
+        pins.test_commit_kv_identity_and_untouched_rows()
+        return True
+    except (AssertionError, IndexError, ValueError):
+        return False
+
+
+def test_pristine_python_oracle_passes_the_pins():
+    assert _py_pins_pass()
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_python_mistake_is_caught(monkeypatch, name):
+    import inspect
+    import textwrap
+
+    fn_name, old, new = PY_MUTANTS[name]
+    src = inspect.getsource(getattr(oracle, fn_name))
+    assert src.count(old) == 1, f"mutant {name}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(textwrap.dedent(src.replace(old, new)), ns)
+    monkeypatch.setattr(oracle, fn_name, ns[fn_name])
+    assert not _py_pins_pass(), f"pins did not catch mutant {name}"

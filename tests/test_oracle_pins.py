@@ -383,3 +383,136 @@ def test_draft_block_masks():
     assert words_iso == [0x0F] * 4 + [0xF0] * 4
     assert words_cau == [0x0F] * 4 + [0xFF] * 4
     assert np.array_equal(oracle.words_to_bool(W.pack_bits(cau), 8), cau)
+
+
+# ----------------------------------------------------------------------------
+# greedy acceptance and KV commit
+# ----------------------------------------------------------------------------
+
+def test_greedy_accept_hand():
+    with open(os.path.join(GOLD, "greedy_accept_hand.json")) as f:
+        g = json.load(f)
+    path, n, bonus = oracle.greedy_accept(np.array(g["parent"], np.int32), np.array(g["draft_tokens"], np.int32),
+                                          np.array(g["target_next"], np.int32))
+    assert path.tolist() == g["path"]
+    assert n.tolist() == g["n_accept"]
+    assert bonus.tolist() == g["bonus"]
+
+
+def _accept_brute_force(parent, draft, tgt):
+    """Every root path of the tree, taken whole: accepted when each of its nodes
+    carries the target's token after its predecessor (the prefix for the first)."""
+    T = len(parent)
+    best = []
+    for end in range(T):
+        nodes = []
+        t = end
+        while t >= 0:
+            nodes.append(t)
+            t = parent[t]
+        nodes = nodes[::-1]
+        prev = -1
+        good = True
+        for t in nodes:
+            if draft[t] != tgt[prev + 1]:
+                good = False
+                break
+            prev = t
+        if good and len(nodes) > len(best):  # ends scanned in increasing order: ties keep the smaller end
+            best = nodes
+    bonus = tgt[best[-1] + 1] if best else tgt[0]
+    return best, bonus
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_greedy_accept_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    B, T = 3, int(rng.integers(1, 13))
+    parent = np.stack([W.random_parents(T, rng) for _ in range(B)]).astype(np.int32)
+    vocab = int(rng.integers(2, 5))  # small vocabulary: many matches, ties between siblings
+    draft = rng.integers(0, vocab, size=(B, T)).astype(np.int32)
+    tgt = rng.integers(0, vocab, size=(B, T + 1)).astype(np.int32)
+    path, n, bonus = oracle.greedy_accept(parent, draft, tgt)
+    for b in range(B):
+        want, wb = _accept_brute_force(parent[b].tolist(), draft[b].tolist(), tgt[b].tolist())
+        assert n[b] == len(want) and path[b, : n[b]].tolist() == want
+        assert np.all(path[b, n[b]:] == -1)
+        assert bonus[b] == wb
+
+
+def test_greedy_accept_chain_is_prefix_match():
+    """On a chain the committed length is the first position where draft and
+    target disagree (the usual greedy speculative decoding rule)."""
+    rng = np.random.default_rng(5)
+    T = 9
+    parent = np.array([W.chain_parents(T)] * 4, np.int32)
+    tgt = rng.integers(0, 100, size=(4, T + 1)).astype(np.int32)
+    draft = tgt[:, :T].copy()
+    for b, m in enumerate([0, 3, 8, T]):  # first mismatch at m (T: none)
+        if m < T:
+            draft[b, m] += 1
+    path, n, bonus = oracle.greedy_accept(parent, draft, tgt)
+    assert n.tolist() == [0, 3, 8, T]
+    for b, m in enumerate([0, 3, 8, T]):
+        assert path[b, :m].tolist() == list(range(m))
+        assert bonus[b] == tgt[b, m]
+
+
+def test_commit_kv_hand():
+    with open(os.path.join(GOLD, "commit_kv_hand.json")) as f:
+        g = json.load(f)
+    rows = np.array(g["rows_before"], np.float32)[None, :, None, :]  # [B=1][slots][Hkv=1][D=2]
+    k, v, L = oracle.commit_kv_dense(rows, rows + 100, np.array([g["seqlen"]], np.int32),
+                                     np.array([g["path"]], np.int32), np.array([g["n_accept"]], np.int32))
+    assert k[0, :, 0].tolist() == g["rows_after"]
+    assert (v - 100)[0, :, 0].tolist() == g["rows_after"]
+    assert L.tolist() == [g["seqlen_after"]]
+
+
+def test_commit_kv_paged_equals_dense():
+    """Committing through a page table and re-reading the sequence equals
+    committing the contiguous copy of the same sequence (HiSpec 2: paged =
+    contiguous)."""
+    rng = np.random.default_rng(11)
+    B, Hkv, D, T, ps = 3, 2, 4, 6, 4
+    L = np.array([5, 0, 9], np.int32)
+    need = (L + T + ps - 1) // ps
+    P = int(need.sum()) + 2
+    perm = rng.permutation(P)
+    table = np.full((B, int(need.max())), -1, np.int32)
+    off = 0
+    for b in range(B):
+        table[b, : need[b]] = perm[off: off + need[b]]
+        off += need[b]
+    kp = rng.standard_normal((P, ps, Hkv, D)).astype(np.float32)
+    vp = rng.standard_normal((P, ps, Hkv, D)).astype(np.float32)
+    parent = np.stack([W.random_parents(T, rng) for _ in range(B)]).astype(np.int32)
+    tgt = rng.integers(0, 2, size=(B, T + 1)).astype(np.int32)
+    draft = rng.integers(0, 2, size=(B, T)).astype(np.int32)
+    path, n, _ = oracle.greedy_accept(parent, draft, tgt)
+    k2, v2, L2 = oracle.commit_kv_paged(kp, vp, table, ps, L, path, n)
+    for b in range(B):
+        cap = int(L[b]) + T
+        kd = oracle.gather_pages(kp, table[b], cap, ps)[None]
+        vd = oracle.gather_pages(vp, table[b], cap, ps)[None]
+        kc, vc, Lc = oracle.commit_kv_dense(kd, vd, L[b:b + 1], path[b:b + 1], n[b:b + 1])
+        assert np.array_equal(oracle.gather_pages(k2, table[b], cap, ps), kc[0])
+        assert np.array_equal(oracle.gather_pages(v2, table[b], cap, ps), vc[0])
+        assert L2[b] == Lc[0] == L[b] + n[b]
+
+
+def test_commit_kv_identity_and_untouched_rows():
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((2, 20, 3, 4)).astype(np.float32)
+    L = np.array([7, 10], np.int32)
+    ident = np.array([[0, 1, 2, -1], [0, 1, -1, -1]], np.int32)
+    k2, _, L2 = oracle.commit_kv_dense(k, k, L, ident, np.array([3, 2], np.int32))
+    assert np.array_equal(k2, k) and L2.tolist() == [10, 12]
+    moved = np.array([[2, 3, -1, -1], [1, -1, -1, -1]], np.int32)
+    k3, _, _ = oracle.commit_kv_dense(k, k, L, moved, np.array([2, 1], np.int32))
+    assert np.array_equal(k3[0, 7], k[0, 9]) and np.array_equal(k3[0, 8], k[0, 10])
+    assert np.array_equal(k3[1, 10], k[1, 11])
+    changed = np.zeros(k.shape[:2], bool)
+    changed[0, 7:9] = True
+    changed[1, 10] = True
+    assert np.array_equal(k3[~changed], k[~changed])
