@@ -222,6 +222,54 @@ va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float
                              int m_draft, int budget, int32_t *indices, int32_t *n_indices,
                              void *workspace, va_stream stream);
 
+/*
+ * After verification (Dustin section 1, step 5: accepted tokens join the
+ * cache, rejected ones are dropped; HiSpec section 2: the entries of rejected
+ * tokens are removed before the next phase, and the output equals the target
+ * model's own decoding).
+ *
+ * Greedy acceptance over token trees.  parent [B][T] int32 as for the
+ * attention calls; draft_tokens [B][T] int32; target_next [B][T+1] int32:
+ * column 0 is the target model's greedy next token after the committed
+ * prefix, column t+1 the one after draft node t.  A node is accepted when its
+ * parent is accepted (or it is a child of the prefix, parent -1) and its token
+ * equals the target's token after that parent.  Outputs, all device int32:
+ * path [B][T] -- the deepest accepted root path as node indices from the root
+ * down (the one ending at the smallest node index when several are equally
+ * deep), tail -1; n_accept [B] -- its length (0 when no node is accepted);
+ * bonus [B] -- the target's token after the path's last node (column 0 when
+ * nothing is accepted).  1 <= T <= 64.  A parent entry that breaks
+ * -1 <= parent[i] < i is recorded as VA_ERR_DEVICE_BOUNDS in the status word
+ * of `workspace` (may be NULL) and that node counts as rejected.
+ */
+va_status verify_accept_greedy(int B, int T, const int32_t *parent, const int32_t *draft_tokens,
+                               const int32_t *target_next, int32_t *path, int32_t *n_accept, int32_t *bonus,
+                               void *workspace, va_stream stream);
+
+/*
+ * KV commit after acceptance, in place.  The draft rows of sequence b sit at
+ * logical slots L_b .. L_b+T-1 (L_b = seqlens[b]); for j < n_accept[b] the
+ * row at slot L_b + path[b][j] is moved to slot L_b + j, in every kv-head of
+ * both caches.  Other slots keep their rows (those past L_b + n_accept[b]
+ * are free for the next step).  path and n_accept as returned by
+ * verify_accept_greedy: path[b][j] in [j, T).  seqlens_out [B] (may be NULL,
+ * must not alias seqlens) receives L_b + n_accept[b].  shape supplies B, T
+ * (<= 64), Hkv, D and dtype (Hq and scale are not used); rows of D elements
+ * must be a multiple of 16 bytes.  Dense: caches [B][max_cache_len][Hkv][D],
+ * L_b + T <= max_cache_len.  Paged: pages [num_pages][page_size][Hkv][D]
+ * behind page_table [B][max_pages_per_seq] as for verify_attn_paged.  Caches
+ * 16-byte aligned.  A seqlen, n_accept, path entry or page entry out of range
+ * is recorded as VA_ERR_DEVICE_BOUNDS in `workspace` (may be NULL); the rows
+ * it concerns are left in place.
+ */
+va_status verify_commit_kv_dense(const va_shape *shape, void *k_cache, void *v_cache, int max_cache_len,
+                                 const int32_t *seqlens, const int32_t *path, const int32_t *n_accept,
+                                 int32_t *seqlens_out, void *workspace, va_stream stream);
+va_status verify_commit_kv_paged(const va_shape *shape, void *k_pages, void *v_pages, int num_pages,
+                                 int page_size, const int32_t *page_table, int max_pages_per_seq,
+                                 const int32_t *seqlens, const int32_t *path, const int32_t *n_accept,
+                                 int32_t *seqlens_out, void *workspace, va_stream stream);
+
 /* Wait for `stream`, read and clear the device status word of `workspace`.
  * Returns VA_OK or the first device-side error recorded since the last check. */
 va_status verify_attn_check_status(void *workspace, va_stream stream);

@@ -7,12 +7,15 @@ from .api import (  # noqa: F401
     VerifyAttnError,
     Workspace,
     make_shape,
+    verify_accept_greedy,
     verify_attn_check_status,
     verify_attn_combine,
     verify_attn_dense,
     verify_attn_paged,
     verify_attn_sparse,
     verify_build_index,
+    verify_commit_kv_dense,
+    verify_commit_kv_paged,
     verify_tree_mask_from_parents,
     version,
     workspace_size,

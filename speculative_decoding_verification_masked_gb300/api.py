@@ -52,6 +52,9 @@ _SIGS = {
     "verify_attn_combine": (_I, [_I, _I, _I, _P, _P, _I, _P, _P, _P]),
     "verify_tree_mask_from_parents": (_I, [_I, _I, _P, _P, _P, _P]),
     "verify_build_index": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "verify_accept_greedy": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "verify_commit_kv_dense": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "verify_commit_kv_paged": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
     "verify_attn_check_status": (_I, [_P, _P]),
     "verify_attn_last_error": (ctypes.c_char_p, []),
     "verify_attn_version": (ctypes.c_char_p, []),
@@ -251,6 +254,53 @@ def verify_build_index(seqlens, score_draft, score_target, n_sink, window, m_dra
                                     window, m_draft, budget, _ptr(indices), _ptr(n_indices),
                                     workspace.ptr if workspace is not None else None, _stream(stream)))
     return indices, n_indices
+
+
+def verify_accept_greedy(parent, draft_tokens, target_next, path=None, n_accept=None, bonus=None,
+                         workspace: Workspace = None, stream=None):
+    """Greedy tree acceptance: returns (path int32 [B][T], n_accept int32 [B], bonus int32 [B])."""
+    B, T = parent.shape
+    dev = parent.device
+    if path is None:
+        path = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if n_accept is None:
+        n_accept = torch.empty(B, dtype=torch.int32, device=dev)
+    if bonus is None:
+        bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib().verify_accept_greedy(B, T, _ptr(parent), _ptr(draft_tokens), _ptr(target_next), _ptr(path),
+                                      _ptr(n_accept), _ptr(bonus), workspace.ptr if workspace is not None else None,
+                                      _stream(stream)))
+    return path, n_accept, bonus
+
+
+def verify_commit_kv_dense(k_cache, v_cache, seqlens, path, n_accept, seqlens_out=None,
+                           workspace: Workspace = None, stream=None):
+    """Move the accepted draft rows of k_cache / v_cache [B][len][Hkv][D] in
+    place to the slots after each prefix; returns seqlens + n_accept."""
+    B, cap, Hkv, D = k_cache.shape
+    T = path.shape[1]
+    if seqlens_out is None:
+        seqlens_out = torch.empty(B, dtype=torch.int32, device=k_cache.device)
+    shape = make_shape(B, T, Hkv, Hkv, D, _dtype_code(k_cache), 1.0)
+    _check(lib().verify_commit_kv_dense(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), cap, _ptr(seqlens),
+                                        _ptr(path), _ptr(n_accept), _ptr(seqlens_out),
+                                        workspace.ptr if workspace is not None else None, _stream(stream)))
+    return seqlens_out
+
+
+def verify_commit_kv_paged(k_pages, v_pages, page_table, seqlens, path, n_accept, seqlens_out=None,
+                           workspace: Workspace = None, stream=None):
+    """The same commit through a page table; pages [P][page][Hkv][D]."""
+    P, ps, Hkv, D = k_pages.shape
+    B, max_pages = page_table.shape
+    T = path.shape[1]
+    if seqlens_out is None:
+        seqlens_out = torch.empty(B, dtype=torch.int32, device=k_pages.device)
+    shape = make_shape(B, T, Hkv, Hkv, D, _dtype_code(k_pages), 1.0)
+    _check(lib().verify_commit_kv_paged(ctypes.byref(shape), _ptr(k_pages), _ptr(v_pages), P, ps, _ptr(page_table),
+                                        max_pages, _ptr(seqlens), _ptr(path), _ptr(n_accept), _ptr(seqlens_out),
+                                        workspace.ptr if workspace is not None else None, _stream(stream)))
+    return seqlens_out
 
 
 def verify_attn_check_status(workspace: Workspace, stream=None):

@@ -293,6 +293,39 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
 
 }  // namespace
 
+namespace {
+va_status commit_common(const va_shape *shape, void *k, void *v, const int32_t *seqlens, const int32_t *path,
+                        const int32_t *n_accept, int32_t *seqlens_out, void *workspace, va::CommitParams &cp) {
+  if (shape == nullptr) return fail(VA_ERR_INVALID_ARG, "shape is NULL");
+  if (shape->B < 1 || shape->T < 1 || shape->Hkv < 1) return fail(VA_ERR_INVALID_ARG, "B, T and Hkv must be >= 1");
+  if (shape->T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d; at most 64 draft tokens are supported", shape->T);
+  if (shape->dtype != VA_DTYPE_BF16 && shape->dtype != VA_DTYPE_FP32)
+    return fail(VA_ERR_INVALID_ARG, "unknown dtype %d", (int)shape->dtype);
+  const int es = shape->dtype == VA_DTYPE_BF16 ? 2 : 4;
+  if (shape->D < 1 || (shape->D * es) % 16 != 0 || shape->D * es > 1024)
+    return fail(VA_ERR_UNSUPPORTED, "rows of D=%d elements must be a multiple of 16 bytes, at most 1 KB", shape->D);
+  if (k == nullptr || v == nullptr || seqlens == nullptr || path == nullptr || n_accept == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "caches, seqlens, path and n_accept must not be NULL");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(VA_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  if (seqlens_out != nullptr && seqlens_out == seqlens)
+    return fail(VA_ERR_INVALID_ARG, "seqlens_out must not alias seqlens");
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  memset(&cp, 0, sizeof cp);
+  cp.B = shape->B;
+  cp.T = shape->T;
+  cp.Hkv = shape->Hkv;
+  cp.row_bytes = shape->D * es;
+  cp.k = k;
+  cp.v = v;
+  cp.seqlens = seqlens;
+  cp.path = path;
+  cp.n_accept = n_accept;
+  cp.seqlens_out = seqlens_out;
+  cp.status = static_cast<int *>(workspace);
+  return VA_OK;
+}
+}  // namespace
+
 extern "C" {
 
 size_t verify_attn_workspace_size(const va_shape *shape) {
@@ -413,6 +446,60 @@ va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float
                                          m_draft, budget, indices, n_indices, static_cast<int *>(workspace),
                                          (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "index launch");
+  return ok();
+}
+
+va_status verify_accept_greedy(int B, int T, const int32_t *parent, const int32_t *draft_tokens,
+                               const int32_t *target_next, int32_t *path, int32_t *n_accept, int32_t *bonus,
+                               void *workspace, va_stream stream) {
+  if (B < 1 || T < 1) return fail(VA_ERR_INVALID_ARG, "B and T must be >= 1");
+  if (T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d; at most 64 draft tokens are supported", T);
+  if (parent == nullptr || draft_tokens == nullptr || target_next == nullptr || path == nullptr ||
+      n_accept == nullptr || bonus == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "parent, draft_tokens, target_next, path, n_accept and bonus must not be NULL");
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaError_t e = va::launch_accept_greedy(B, T, parent, draft_tokens, target_next, path, n_accept, bonus,
+                                           static_cast<int *>(workspace), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
+  return ok();
+}
+
+
+va_status verify_commit_kv_dense(const va_shape *shape, void *k_cache, void *v_cache, int max_cache_len,
+                                 const int32_t *seqlens, const int32_t *path, const int32_t *n_accept,
+                                 int32_t *seqlens_out, void *workspace, va_stream stream) {
+  va::CommitParams cp;
+  va_status st = commit_common(shape, k_cache, v_cache, seqlens, path, n_accept, seqlens_out, workspace, cp);
+  if (st != VA_OK) return st;
+  if (max_cache_len < shape->T)
+    return fail(VA_ERR_INVALID_ARG, "max_cache_len=%d is smaller than T=%d", max_cache_len, shape->T);
+  cp.len_cap = max_cache_len;
+  cudaError_t e = va::launch_commit_kv(cp, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  return ok();
+}
+
+va_status verify_commit_kv_paged(const va_shape *shape, void *k_pages, void *v_pages, int num_pages, int page_size,
+                                 const int32_t *page_table, int max_pages_per_seq, const int32_t *seqlens,
+                                 const int32_t *path, const int32_t *n_accept, int32_t *seqlens_out,
+                                 void *workspace, va_stream stream) {
+  va::CommitParams cp;
+  va_status st = commit_common(shape, k_pages, v_pages, seqlens, path, n_accept, seqlens_out, workspace, cp);
+  if (st != VA_OK) return st;
+  if (page_table == nullptr) return fail(VA_ERR_INVALID_ARG, "page_table must not be NULL");
+  if (page_size < 1 || page_size > 1024 || (page_size & (page_size - 1)) != 0)
+    return fail(VA_ERR_INVALID_ARG, "page_size=%d must be a power of two in [1, 1024]", page_size);
+  if (num_pages < 1 || max_pages_per_seq < 1) return fail(VA_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
+  const long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap < shape->T || cap >= (1ll << 31))
+    return fail(VA_ERR_INVALID_ARG, "max_pages_per_seq * page_size = %lld must be in [T, 2^31)", cap);
+  cp.len_cap = (int)cap;
+  cp.page_table = page_table;
+  cp.num_pages = num_pages;
+  cp.max_pages = max_pages_per_seq;
+  while ((1 << cp.page_shift) < page_size) ++cp.page_shift;
+  cudaError_t e = va::launch_commit_kv(cp, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   return ok();
 }
 
