@@ -202,6 +202,61 @@ def per_call_durations(cases, n_calls):
     return [a.elapsed_time(b) * 1e-3 for a, b in ev]
 
 
+def measure_next_rows(va, peak, steps=1024):
+    """The steps after verification at the paged workload's shape (B64, T16
+    random trees, 16-row pages): greedy acceptance, then the KV commit of the
+    accepted rows.  Device time per call from CUDA events around graphs of 64
+    calls; the commit's bytes are the rows it moves, read once and written once."""
+    w = W.make_workload("paged", seed=0, tree="random")
+    rng = np.random.default_rng(1)
+    # tokens from a 2-symbol alphabet: paths of a few nodes, some rows moved
+    tgt = rng.integers(0, 2, size=(w.B, w.T + 1)).astype(np.int32)
+    draft = rng.integers(0, 2, size=(w.B, w.T)).astype(np.int32)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+    parent, d_draft, d_tgt = i32(w.parent), i32(draft), i32(tgt)
+    k, v, table, seqlens = w.k_pages.cuda(), w.v_pages.cuda(), i32(w.page_table), i32(w.seqlens)
+    path, n, bonus = va.verify_accept_greedy(parent, d_draft, d_tgt)
+    seq_out = torch.empty_like(seqlens)
+    torch.cuda.synchronize()
+    p_h, n_h = path.cpu().numpy(), n.cpu().numpy()
+    moved = int(sum(int(np.sum(p_h[b, : n_h[b]] != np.arange(n_h[b]))) for b in range(w.B)))
+    row_bytes = w.D * 2
+    commit_bytes = moved * w.Hkv * 2 * row_bytes * 2
+    res = {"workload": f"paged shape: B{w.B} T{w.T} Hkv{w.Hkv} d{w.D} bf16, random trees, 16-row pages",
+           "mean_accepted": round(float(n_h.mean()), 2), "rows_moved_per_call": moved * w.Hkv * 2}
+
+    def timed(fn):
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(64):
+                fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // 64)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / (reps * 64)
+
+    t_acc = timed(lambda: va.verify_accept_greedy(parent, d_draft, d_tgt, path=path, n_accept=n, bonus=bonus))
+    # the same accepted rows are moved every call (the cache content changes, the traffic does not)
+    t_com = timed(lambda: va.verify_commit_kv_paged(k, v, table, seqlens, path, n, seqlens_out=seq_out))
+    res["accept_us"] = round(t_acc * 1e6, 3)
+    res["commit_us"] = round(t_com * 1e6, 3)
+    res["commit_GBps"] = round(commit_bytes / t_com / 1e9, 1)
+    res["commit_frac_of_measured_hbm"] = round(commit_bytes / t_com / 1e9 / peak, 4)
+    res["note"] = "both latency-bound at this size: a few KB per sequence"
+    return res
+
+
 def e2e_measure(w, va, steps):
     """Through the public API with host buffers: per step H2D the new inputs from
     pinned memory, run the call, D2H out and lse, and wait for them."""
@@ -372,6 +427,21 @@ def run_profile(args):
 
     torch.cuda.set_device(0)
     va.api.lib(build_if_missing=False)
+    if args.profile == "after":
+        w = W.make_workload("paged", seed=0, tree="random")
+        rng = np.random.default_rng(1)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+        tgt = i32(rng.integers(0, 2, size=(w.B, w.T + 1)))
+        draft = i32(rng.integers(0, 2, size=(w.B, w.T)))
+        k, v = w.k_pages.cuda(), w.v_pages.cuda()
+        ws = va.Workspace(256)
+        for _ in range(args.calls):
+            path, n, _ = va.verify_accept_greedy(i32(w.parent), draft, tgt, workspace=ws)
+            va.verify_commit_kv_paged(k, v, i32(w.page_table), i32(w.seqlens), path, n, workspace=ws)
+        torch.cuda.synchronize()
+        va.verify_attn_check_status(ws)
+        print(json.dumps({"profile": "after", "calls": args.calls, "status": "ok"}))
+        return 0
     case = DeviceCase(W.make_workload(args.profile, seed=0), va)
     for _ in range(args.calls):
         case.step()
@@ -495,8 +565,9 @@ def main():
     ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES), default=None,
-                    help="run --calls plain verification steps of one workload (for ncu) and exit")
+    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after"], default=None,
+                    help="run --calls plain verification steps of one workload (for ncu) and exit; "
+                         "'after': --calls acceptance + KV commit pairs at the paged shape")
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -522,6 +593,7 @@ def main():
             others[name] = {"GBps": round(r["gbs"] / world, 1), "frac_of_measured_hbm": round(r["gbs"] / world / peak, 4),
                             "us_per_step": round(r["dt"] * 1e6, 2), "tokens_per_s": round(r["tok_s"] / world, 1),
                             "call_us": round(r["call_s"] * 1e6, 2)}
+    next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -563,6 +635,8 @@ def main():
         line["cpu_baseline"] = main_res["cpu"]
     if others:
         line["other_configs"] = others
+    if next_rows is not None:
+        line["after_verification"] = next_rows
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -14,6 +14,7 @@
 
 #include "va_common.cuh"
 #include "va_kernels.h"
+#include "va_commit.h"
 #include "verify_attn_testing.h"
 
 namespace {

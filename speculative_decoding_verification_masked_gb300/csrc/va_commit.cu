@@ -14,6 +14,7 @@
 //    reads a row it has already overwritten.
 #include "va_common.cuh"
 #include "va_kernels.h"
+#include "va_commit.h"
 
 namespace va {
 

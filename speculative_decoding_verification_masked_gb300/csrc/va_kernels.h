@@ -69,21 +69,4 @@ cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const flo
                                int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t wait_ns, cudaStream_t stream);
 
-// after verification: greedy acceptance and the KV commit (va_commit.cu)
-cudaError_t launch_accept_greedy(int B, int T, const int32_t *parent, const int32_t *draft,
-                                 const int32_t *target_next, int32_t *path, int32_t *n_accept, int32_t *bonus,
-                                 int *status, cudaStream_t stream);
-struct CommitParams {
-  int B, T, Hkv;
-  int row_bytes;                // D * element size (a multiple of 16)
-  void *k, *v;                  // dense [B][len_cap][Hkv][D] or paged [P][page][Hkv][D]
-  int len_cap;                  // dense: max_cache_len; paged: max_pages * page size
-  const int32_t *page_table;    // nullptr for the dense cache
-  int page_shift, max_pages, num_pages;
-  const int32_t *seqlens, *path, *n_accept;
-  int32_t *seqlens_out;         // may be nullptr
-  int *status;                  // may be nullptr
-};
-cudaError_t launch_commit_kv(const CommitParams &p, cudaStream_t stream);
-
 }  // namespace va
