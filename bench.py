@@ -470,11 +470,20 @@ def barrier(dist):
 
 
 def max_over_ranks(x, dist):
+    """The slowest rank's value (NCCL reduces device tensors, gloo host ones)."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank, seconds, dist):
+    """Units every rank processed, over the slowest rank's time (weak scaling:
+    each rank runs its own replica of the workload)."""
+    world = dist.get_world_size() if dist is not None else 1
+    return units_per_rank * world / max_over_ranks(seconds, dist)
 
 
 def run_reference(args):
@@ -538,7 +547,7 @@ def measure_config(name, va, args, want_e2e, want_cpu, rank, dist):
     dt_max = max_over_ranks(dt, dist)
     world = dist.get_world_size() if dist is not None else 1
     bytes_step = w.kv_bytes()
-    gbs = bytes_step * world / dt_max / 1e9
+    gbs = whole_job_rate(bytes_step, dt, dist) / 1e9
     durs = per_call_durations(cases, 200)
     call_s = statistics.mean(durs)
     res = {"w": w, "dt": dt_max, "gbs": gbs, "tok_s": w.tokens() * world / dt_max, "call_s": call_s,
