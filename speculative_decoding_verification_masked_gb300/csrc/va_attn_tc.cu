@@ -14,7 +14,7 @@
 //                    O in TMEM when the row max grows by more than 2^8, and
 //                    writes the output row.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
-//                    sparse) into a 4-stage ring (shared with the other kernel)
+//                    sparse) into a 3-stage ring (shared with the other kernel)
 //   warps 4*NMT+1+i  PV issuer of M-tile i: O_i += P_i V (A = P from TMEM, B =
 //                    V as an MN-major operand).  Issuer 0 owns the TMEM
 //                    allocation.
@@ -38,7 +38,7 @@
 
 namespace va {
 
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 3;
 
 // ---------------------------------------------------------------------------
 // shared memory plan
@@ -49,7 +49,7 @@ struct TcSmem {
   static constexpr int kStageBytes = StageGeom<__nv_bfloat16, 128>::kStageBytes;
   static constexpr int kStagesOff = kQBytes;
   static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
-  // barriers: full[4], empty[4], s_full[2][2], p_full[2][2], o_done[2][2], drain
+  // barriers: full[NS], empty[NS], s_full[2][2], p_full[2][2], o_done[2][2], drain
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kTstartOff = kMiscOff + 16;
@@ -341,29 +341,19 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
       const float m_new = fmaxf(m_used, mx);
+      // move the reference max only when it grew by more than 2^8 (exact either
+      // way); O is rescaled below, once P is written and the scores are dead
+      bool rescale = false;
+      float alpha = 1.f;
       if (lt == lt0) {
         m_used = m_new;
       } else {
-        // move the reference max only when it grew by more than 2^8 (exact either way)
         const bool need = (m_new - m_used) * cl2 > 8.f;
-        if (__any_sync(0xffffffffu, need)) {
-          wait_ok(o_done + 2 * mi + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);  // O holds every PV up to tile jt-1
-          tc_fence_after();
-          const float alpha = need ? exp2f((m_used - m_new) * cl2) : 1.f;
-#pragma unroll
-          for (int cch = 0; cch < 4; ++cch) {
-            uint32_t u[32];
-            tmem_ld32(tO + 32 * cch, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
-            tmem_st32(tO + 32 * cch, u);
-          }
-          tmem_st_wait();
-          if (need) {
-            l *= alpha;
-            m_used = m_new;
-          }
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = exp2f((m_used - m_new) * cl2);
+          l *= alpha;
+          m_used = m_new;
         }
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
@@ -393,6 +383,21 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       }
       const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l += ls;
+      if (rescale) {
+        // O relative to the new reference before PV(jt) adds to it; O holds
+        // every PV up to tile jt-1 once that one has completed
+        wait_ok(o_done + 2 * mi + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);
+        tc_fence_after();
+#pragma unroll
+        for (int cch = 0; cch < 4; ++cch) {
+          uint32_t u[32];
+          tmem_ld32(tO + 32 * cch, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+          tmem_st32(tO + 32 * cch, u);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full + 2 * mi + b);
