@@ -55,6 +55,7 @@ constexpr int kIdxCacheKeys = 36864;  // keys held in shared memory when L fits
 constexpr int kIdxLoads = 16;         // score loads in flight per thread while caching
 constexpr int kIdxBins = 2048;        // bins of one radix digit (11 bits)
 constexpr int kIdxCopies = 8;         // histogram copies, each shared by 4 warps
+constexpr int kIdxCandCap = (kIdxCopies - 1) * kIdxBins;  // candidate keys held behind one histogram
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -125,7 +126,7 @@ __device__ __forceinline__ void hist_zero(const IdxSmem &sm) {
 // The bucket of digit d that holds the kk-th largest counted key: thread t
 // owns the 1 or 2 bins just below bin 2047 - per * t (bins scanned from the
 // top).  Sets scratch[64] = bin, [65] = rank inside it, [66] = bucket taken whole.
-__device__ __forceinline__ void find_bucket(int d, int kk, const IdxSmem &sm) {
+__device__ __forceinline__ void find_bucket(int d, int kk, const IdxSmem &sm, int copies) {
   const int nb = 1 << digit_bits(d);
   const int per = nb / kIdxThreads;  // 2 or 1
   const int tid = threadIdx.x;
@@ -134,8 +135,7 @@ __device__ __forceinline__ void find_bucket(int d, int kk, const IdxSmem &sm) {
   for (int j = 0; j < 2; ++j) {
     if (j < per) {
       const int bin = nb - 1 - (tid * per + j);
-#pragma unroll
-      for (int h = 0; h < kIdxCopies; ++h) c[j] += (int)sm.hist[h * kIdxBins + bin];
+      for (int h = 0; h < copies; ++h) c[j] += (int)sm.hist[h * kIdxBins + bin];
     }
   }
   int tot;
@@ -215,9 +215,23 @@ __device__ Take select_top(const float *src, int L, int k, const IdxSmem &sm, co
   uint32_t prefix = 0, pmask = 0;
   int kk = k;
   bool exact_bucket = false;
+  // after the first digit the keys of its chosen bucket are copied to a
+  // candidate list (behind the first histogram), and the later digits count
+  // those only, with one histogram; a bucket larger than the list keeps the
+  // full passes
+  uint32_t *cand = sm.hist + kIdxBins;
+  int ncand = -1;
   for (int d = 0; d < 3; ++d) {
     const int shift = digit_shift(d), bits = digit_bits(d);
-    if (d > 0) {
+    if (d > 0 && ncand >= 0) {
+      for (int j = tid; j < kIdxBins; j += kIdxThreads) sm.hist[j] = 0;
+      __syncthreads();
+      for (int e = tid; e < ncand; e += kIdxThreads) {
+        const uint32_t key = cand[e];
+        if ((key & pmask) == prefix) atomicAdd(sm.hist + ((key >> shift) & ((1u << bits) - 1u)), 1u);
+      }
+      __syncthreads();
+    } else if (d > 0) {
       hist_zero(sm);
       __syncthreads();
       for (int base = 0; base < L; base += kIdxThreads * 4) {
@@ -233,13 +247,32 @@ __device__ Take select_top(const float *src, int L, int k, const IdxSmem &sm, co
       }
       __syncthreads();
     }
-    find_bucket(d, kk, sm);
+    find_bucket(d, kk, sm, ncand >= 0 ? 1 : kIdxCopies);
     prefix |= (uint32_t)sm.scratch[64] << shift;
     pmask |= ((1u << bits) - 1u) << shift;
     kk = sm.scratch[65];
     exact_bucket = sm.scratch[66] != 0;
     __syncthreads();
     if (exact_bucket) break;
+    if (d == 0 && cached) {
+      // candidate list: warp-aggregated appends of the keys in the bucket
+      if (tid == 0) sm.scratch[67] = 0;
+      __syncthreads();
+      for (int base = 0; base < L; base += kIdxThreads) {
+        const int i = base + tid;
+        const uint32_t key = i < L ? sm.keys[i] : 0u;
+        const bool in = key != 0u && (key & pmask) == prefix;
+        const uint32_t m = __ballot_sync(0xffffffffu, in);
+        int at = 0;
+        if (lane == 0 && m != 0u) at = atomicAdd(&sm.scratch[67], __popc(m));
+        at = __shfl_sync(0xffffffffu, at, 0) + __popc(m & ((1u << lane) - 1u));
+        if (in && at < kIdxCandCap) cand[at] = key;
+      }
+      __syncthreads();
+      const int n = sm.scratch[67];
+      ncand = n <= kIdxCandCap ? n : -1;
+      __syncthreads();
+    }
   }
   if (exact_bucket) {
     const Take t{prefix, pmask, true};
