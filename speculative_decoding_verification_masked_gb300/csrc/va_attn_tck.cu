@@ -239,10 +239,10 @@ __device__ __forceinline__ void merge_rows_warp(const AttnParams &p, int s, int 
 #pragma unroll
       for (int j = 0; j < MB; ++j) {
         const bool in = q0 + j < np;
-        ls[j] = in ? __ldg(l + (size_t)(q0 + j) * p.rows_pad) : -INFINITY;
+        ls[j] = in ? __ldcg(l + (size_t)(q0 + j) * p.rows_pad) : -INFINITY;  // written by other CTAs: L2
 #pragma unroll
         for (int c = 0; c < C4; ++c)
-          v[j][c] = in ? __ldg(reinterpret_cast<const float4 *>(o + (size_t)(q0 + j) * ostride) + c)
+          v[j][c] = in ? __ldcg(reinterpret_cast<const float4 *>(o + (size_t)(q0 + j) * ostride) + c)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float m = M;
@@ -718,37 +718,63 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     // column d = tid of O / l for every row, staged row-major in the Q buffer
     // (free: every MMA of this part has completed) and written by bulk copies
     if (n_parts > 1) {
-      // fp32 part: the slot's NR rows are contiguous; two halves of NR/2 rows
       constexpr int HR = NR / 2;
-      float *stage_f = reinterpret_cast<float *>(sQ);
+      if constexpr (NR <= 32) {
+        // fp32 part: thread d stores column d of every row straight from TMEM
+        // (a warp writes 128 contiguous bytes of a row)
+        float *orow = p.o_part + slot * p.rows_pad * D + tid;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float ov[HR];
-        tmem_ld_f<HR>(tO + half * HR, ov);
+        for (int half = 0; half < 2; ++half) {
+          float ov[HR];
+          tmem_ld_f<HR>(tO + half * HR, ov);
+          if (ok) {
 #pragma unroll
-        for (int j = 0; j < HR; j += 4) {
-          const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + half * HR + j);
-          stage_f[(j + 0) * D + tid] = ov[j] * inv4.x;
-          stage_f[(j + 1) * D + tid] = ov[j + 1] * inv4.y;
-          stage_f[(j + 2) * D + tid] = ov[j + 2] * inv4.z;
-          stage_f[(j + 3) * D + tid] = ov[j + 3] * inv4.w;
+            for (int j = 0; j < HR; j += 4) {
+              const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + half * HR + j);
+              orow[(half * HR + j + 0) * D] = ov[j] * inv4.x;
+              orow[(half * HR + j + 1) * D] = ov[j + 1] * inv4.y;
+              orow[(half * HR + j + 2) * D] = ov[j + 2] * inv4.z;
+              orow[(half * HR + j + 3) * D] = ov[j + 3] * inv4.w;
+            }
+          }
         }
-        fence_proxy_async_smem();
+        // publish the part (always, also after a failed wait, so the counters
+        // return to zero): the block barrier orders every thread's row and lse
+        // stores before thread 0's release increment, which is cumulative
         named_bar_sync(kBarSoft, kSoft);
-        if (tid == 0 && ok) {
-          bulk_store_s2g(p.o_part + (slot * p.rows_pad + half * HR) * D, stage_f, (uint32_t)(HR * D * 4));
-          bulk_commit();
-          bulk_wait_read_all();
+        if (tid == 0) red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+      } else {
+        // 64 rows (registers are short): rows staged row-major in the Q buffer,
+        // two halves of NR/2 rows written by bulk copies
+        float *stage_f = reinterpret_cast<float *>(sQ);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float ov[HR];
+          tmem_ld_f<HR>(tO + half * HR, ov);
+#pragma unroll
+          for (int j = 0; j < HR; j += 4) {
+            const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + half * HR + j);
+            stage_f[(j + 0) * D + tid] = ov[j] * inv4.x;
+            stage_f[(j + 1) * D + tid] = ov[j + 1] * inv4.y;
+            stage_f[(j + 2) * D + tid] = ov[j + 2] * inv4.z;
+            stage_f[(j + 3) * D + tid] = ov[j + 3] * inv4.w;
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(kBarSoft, kSoft);
+          if (tid == 0 && ok) {
+            bulk_store_s2g(p.o_part + (slot * p.rows_pad + half * HR) * D, stage_f, (uint32_t)(HR * D * 4));
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          named_bar_sync(kBarSoft, kSoft);
         }
+        // publish (always): the block barrier orders every thread's lse stores
+        // before thread 0's release, which follows the landing of the bulk rows
         named_bar_sync(kBarSoft, kSoft);
-      }
-      // publish the part (always, also after a failed wait, so the counters
-      // return to zero): the block barrier orders every thread's lse stores
-      // before thread 0's release, which follows the landing of the bulk rows
-      named_bar_sync(kBarSoft, kSoft);
-      if (tid == 0) {
-        bulk_wait_all();
-        red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+        if (tid == 0) {
+          bulk_wait_all();
+          red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+        }
       }
       if (n_split < 2) {
         ms[n_split] = s;
