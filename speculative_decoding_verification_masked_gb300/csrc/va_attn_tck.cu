@@ -180,14 +180,17 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float *a) 
     for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * a[j]);
     tmem_st16(taddr, u);
   } else {
+    // 16 columns at a time, each stored before the next is loaded: this rare
+    // path then needs few registers next to the 64-row softmax state
 #pragma unroll
-    for (int h = 0; h < NR / 32; ++h) {
-      uint32_t u[32];
-      tmem_ld32(taddr + 32 * h, u);
+    for (int h = 0; h < NR / 16; ++h) {
+      uint32_t u[16];
+      tmem_ld16(taddr + 16 * h, u);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * a[32 * h + j]);
-      tmem_st32(taddr + 32 * h, u);
+      for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * a[16 * h + j]);
+      tmem_st16(taddr + 16 * h, u);
+      tmem_st_wait();
     }
   }
 }
