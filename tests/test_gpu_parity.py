@@ -414,3 +414,60 @@ def test_partials_never_read_stale_workspace(case):
     out, lse = run_library(w, "mask" if w.parent is None else "parent", workspace=ws, **kw)
     va.verify_attn_check_status(ws)
     compare(out, lse, ref)
+
+
+# ----------------------------------------------------------------------------
+# the online softmax's reference maximum has to move
+# ----------------------------------------------------------------------------
+
+def _reference_jumps(w):
+    """Key 0 of every sequence and kv-head scores far below the draft rows'
+    usual scores, and every key of the second half of the sequence is shifted
+    along the rows' mean query direction so that its score rises by about 8:
+    the first tile's reference (key 0) has to move at once, and the first tile
+    of the second half moves it again, so O and l are rescaled.  The weight
+    stays spread over the many keys of the second half (a few dominant keys
+    would test the precision of a single bf16 P instead, 2^-9 of each weight)."""
+    q = w.q.float()
+    group = w.Hq // w.Hkv
+    for b in range(w.B):
+        n = int(w.seqlens[b]) + w.T
+        for h in range(w.Hkv):
+            rows = q[b, :, h * group:(h + 1) * group].reshape(-1, w.D)
+            u = rows.sum(0)
+            u = u / u.norm()
+            proj = float((rows @ u).mean())
+            shift = 8.0 * w.D ** 0.5 / max(proj, 0.5)  # mean score rise of about 8
+            slots = [(0, None)] + [(s, 1.0) for s in range(n // 2, n)]
+            for slot, sign in slots:
+                if w.layout == "paged":
+                    ref = w.k_pages[w.page_table[b, slot // w.page_size], slot % w.page_size]
+                else:
+                    ref = w.k_cache[b, slot]
+                if sign is None:
+                    ref[h] = (-shift * u).to(w.q.dtype)
+                else:
+                    ref[h] = (ref[h].float() + shift * u).to(w.q.dtype)
+    return w
+
+
+@pytest.mark.parametrize("case", ["chain", "paged64rows", "tree", "sparse", "tiny_fp32"])
+def test_reference_max_moves(case):
+    if case == "chain":
+        w = W.make_workload("chain", seed=81, B=2, L_lo=1500, L_hi=3000)
+    elif case == "paged64rows":
+        w = W.make_workload("paged", seed=82, B=3, L_lo=800, L_hi=2500, page_size=16)
+    elif case == "tree":
+        w = W.make_workload("tree", seed=83, B=1, Hkv=2, L=2500)
+    elif case == "sparse":
+        w = W.make_workload("sparse", seed=84, B=2, Hkv=2, L_lo=3000, L_hi=5000, budget=600, m_draft=200, window=64)
+    else:
+        w = W.make_workload("tiny", seed=85, L=2000)
+    w = _reference_jumps(w)
+    if w.layout == "sparse":  # the oracle's verify sets, handed to the library
+        ref = oracle.verify(w)
+        out, lse = run_library(w, "parent", indices=dev_i32(ref["indices"]), n_indices=dev_i32(ref["n_indices"]))
+        torch.cuda.synchronize()
+        compare(out, lse, ref)
+    else:
+        _check(w, "mask" if case == "paged64rows" else "parent")
