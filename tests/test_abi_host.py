@@ -91,3 +91,30 @@ def test_paged_sparse_index_mask_combine_argument_checks():
     assert L.verify_attn_combine(4, 0, 128, FAKE, FAKE, 0, FAKE, FAKE, None) == api.VA_ERR_INVALID_ARG
     assert L.verify_attn_combine(4, 2, 96, FAKE, FAKE, 0, FAKE, FAKE, None) == api.VA_ERR_UNSUPPORTED
     assert L.verify_attn_workspace_size(None) == 0
+
+
+def test_acceptance_and_commit_argument_checks():
+    """The after-verification entry points reject bad arguments on the host,
+    before any device work."""
+    L = api.lib()
+    acc = L.verify_accept_greedy
+    assert acc(0, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == api.VA_ERR_INVALID_ARG
+    assert acc(1, 65, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == api.VA_ERR_UNSUPPORTED
+    assert acc(1, 4, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None) == api.VA_ERR_INVALID_ARG
+    assert acc(1, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, None) == api.VA_ERR_WORKSPACE
+    s = _shape()
+    dense = L.verify_commit_kv_dense
+    assert dense(None, FAKE, FAKE, 100, FAKE, FAKE, FAKE, None, None, None) == api.VA_ERR_INVALID_ARG
+    assert dense(ctypes.byref(s), None, FAKE, 100, FAKE, FAKE, FAKE, None, None, None) == api.VA_ERR_INVALID_ARG
+    assert dense(ctypes.byref(s), FAKE + 4, FAKE, 100, FAKE, FAKE, FAKE, None, None, None) == api.VA_ERR_INVALID_ARG
+    assert dense(ctypes.byref(s), FAKE, FAKE, 3, FAKE, FAKE, FAKE, None, None, None) == api.VA_ERR_INVALID_ARG
+    # seqlens_out must not alias seqlens
+    assert dense(ctypes.byref(s), FAKE, FAKE, 100, FAKE + 256, FAKE, FAKE, FAKE + 256, None, None) == \
+        api.VA_ERR_INVALID_ARG
+    big = _shape(T=65)
+    assert dense(ctypes.byref(big), FAKE, FAKE, 100, FAKE, FAKE, FAKE, None, None, None) == api.VA_ERR_UNSUPPORTED
+    paged = L.verify_commit_kv_paged
+    assert paged(ctypes.byref(s), FAKE, FAKE, 10, 12, FAKE, 4, FAKE, FAKE, FAKE, None, None, None) == \
+        api.VA_ERR_INVALID_ARG  # page size not a power of two
+    assert paged(ctypes.byref(s), FAKE, FAKE, 10, 16, None, 4, FAKE, FAKE, FAKE, None, None, None) == \
+        api.VA_ERR_INVALID_ARG  # no page table
