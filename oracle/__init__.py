@@ -21,7 +21,8 @@ explicit key list and the explicit full visibility matrix the C code consumes:
 
 The verify-set selection (Dustin 1, "hybrid attention aggregation") is here
 too, written as a full stable sort of candidates by (score descending, index
-ascending).
+ascending), and so is the importance map of a few query heads that feeds it
+(Dustin 1 and 2), written with numpy in fp64.
 
 Readings where the pages are silent are documented with each function.
 """
@@ -418,6 +419,56 @@ def commit_kv_paged(k_pages, v_pages, page_table, page_size, seqlens, path, n_ac
             k[dp, dr] = np.asarray(k_pages)[sp, sr]
             v[dp, dr] = np.asarray(v_pages)[sp, sr]
     return k, v, (np.asarray(seqlens) + np.asarray(n_accept)).astype(np.int32)
+
+
+# ----------------------------------------------------------------------------
+# importance of the cached positions from a few query heads (Dustin section 1:
+# the target model's attention scores are one of the two signals of the global
+# importance map; section 2: that estimate is computed on a few semantic
+# retrieval heads only, instead of every head of every layer)
+# ----------------------------------------------------------------------------
+
+def _widen(a):
+    """bf16 bit patterns / fp32 / fp64 -> float64, exactly."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def head_importance(q, k_cache, seqlens, heads, scale):
+    """Global importance map of the cached prefix from the listed query heads.
+
+    Reading (the pages name the signal -- attention scores of a few heads --
+    but not how they are pooled): for sequence b with L = seqlens[b], each
+    listed head h and each query token t < T, the attention distribution over
+    the L committed keys,
+        p[h, t][j] = exp(scale q[b,t,h] . k[b,j,h // group])
+                     / sum_{j' < L} exp(scale q[b,t,h] . k[b,j',h // group]),
+    and the importance of position j is the sum of p[h, t][j] over the listed
+    heads and the T tokens (a head listed twice counts twice).  Only the L
+    committed keys are scored: the draft rows after them are no candidates of
+    the verify set.
+
+    q [B][T][Hq][D], k_cache [B][Lmax][Hkv][D] (bf16 bits, fp32 or fp64).
+    Returns f64 [B][Lmax], zero at j >= L.
+    """
+    B, T, Hq, D = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    group = Hq // Hkv
+    imp = np.zeros((B, Lmax))
+    for b in range(B):
+        L = int(seqlens[b])
+        if L == 0:
+            continue
+        for h in heads:
+            qh = _widen(q[b, :, h])                 # [T][D]
+            kh = _widen(k_cache[b, :L, h // group])  # [L][D]
+            z = scale * (qh @ kh.T)                 # [T][L]
+            z = z - z.max(axis=1, keepdims=True)
+            e = np.exp(z)
+            imp[b, :L] += (e / e.sum(axis=1, keepdims=True)).sum(axis=0)
+    return imp
 
 
 # ----------------------------------------------------------------------------

@@ -109,6 +109,13 @@ PY_MUTANTS = {
                        "src = [L + j for j in range(a)]"),
     "commit_paged_row": ("commit_kv_paged", "return int(page_table[b][slot // page_size]), slot % page_size",
                          "return int(page_table[b][slot // page_size]), (slot + 1) % page_size"),
+    "importance_gqa_mapping": ("head_importance", "k_cache[b, :L, h // group]", "k_cache[b, :L, h % Hkv]"),
+    "importance_shifted_rows": ("head_importance", "k_cache[b, :L, h // group]", "k_cache[b, 1:L + 1, h // group]"),
+    "importance_dropped_scale": ("head_importance", "z = scale * (qh @ kh.T)", "z = qh @ kh.T"),
+    "importance_unnormalised": ("head_importance", "(e / e.sum(axis=1, keepdims=True))", "e"),
+    "importance_normalised_over_tokens": ("head_importance", "e / e.sum(axis=1, keepdims=True)",
+                                          "e / e.sum(axis=0, keepdims=True)"),
+    "importance_max_over_tokens": ("head_importance", "z.max(axis=1, keepdims=True)", "z.max(axis=0, keepdims=True)"),
 }
 
 
@@ -122,6 +129,11 @@ def _py_pins_pass():
         pins.test_commit_kv_hand()
         pins.test_commit_kv_paged_equals_dense()
         pins.test_commit_kv_identity_and_untouched_rows()
+        pins.test_head_importance_hand()
+        for seed in range(2):
+            pins.test_head_importance_matches_torch_softmax(seed)
+        pins.test_head_importance_mass_and_equal_keys()
+        pins.test_head_importance_follows_the_prefix_rows_only()
         return True
     except (AssertionError, IndexError, ValueError):
         return False

@@ -516,3 +516,92 @@ def test_commit_kv_identity_and_untouched_rows():
     changed[0, 7:9] = True
     changed[1, 10] = True
     assert np.array_equal(k3[~changed], k[~changed])
+
+
+# ----------------------------------------------------------------------------
+# importance map of a few query heads (the scoring pass that feeds the verify set)
+# ----------------------------------------------------------------------------
+
+def test_head_importance_hand():
+    with open(os.path.join(GOLD, "head_importance_hand.json")) as f:
+        g = json.load(f)
+    q = np.array(g["q"], np.float64)[None]
+    k = np.array(g["k"], np.float64)[None]
+    for case in g["cases"]:
+        imp = oracle.head_importance(q, k, np.array(g["seqlens"], np.int32), case["heads"], g["scale"])
+        assert np.allclose(imp[0], case["importance"], rtol=0.0, atol=1e-12), case["heads"]
+
+
+def _importance_case(seed, B=3, T=4, Hq=8, Hkv=2, D=16, Lmax=40):
+    rng = np.random.default_rng(seed)
+    q = W.bf16_bits(torch.from_numpy(rng.standard_normal((B, T, Hq, D)).astype(np.float32)).to(torch.bfloat16))
+    k = W.bf16_bits(torch.from_numpy(rng.standard_normal((B, Lmax, Hkv, D)).astype(np.float32)).to(torch.bfloat16))
+    L = rng.integers(1, Lmax - T + 1, size=B).astype(np.int32)
+    L[0] = Lmax - T
+    return q, k, L
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_head_importance_matches_torch_softmax(seed):
+    """Against torch's softmax in float64 over einsum scores (library routines)."""
+    q, k, L = _importance_case(seed)
+    heads = [1, 6, 6, 3]
+    scale = 0.3
+    imp = oracle.head_importance(q, k, L, heads, scale)
+    qt, kt = torch.from_numpy(_f64(q)), torch.from_numpy(_f64(k))
+    group = q.shape[2] // k.shape[2]
+    for b in range(len(L)):
+        want = torch.zeros(k.shape[1], dtype=torch.float64)
+        for h in heads:
+            s = torch.einsum("td,ld->tl", qt[b, :, h], kt[b, : L[b], h // group]) * scale
+            want[: L[b]] += torch.softmax(s, dim=-1).sum(dim=0)
+        assert np.allclose(imp[b], want.numpy(), rtol=0.0, atol=1e-12)
+
+
+def test_head_importance_single_head_and_token_is_scipy_softmax():
+    scipy_special = pytest.importorskip("scipy.special")
+    q, k, L = _importance_case(7, T=1)
+    for h in range(q.shape[2]):
+        imp = oracle.head_importance(q, k, L, [h], 0.25)
+        for b in range(len(L)):
+            kv = h // (q.shape[2] // k.shape[2])
+            want = scipy_special.softmax(0.25 * (_f64(k[b, : L[b], kv]) @ _f64(q[b, 0, h])))
+            assert np.allclose(imp[b, : L[b]], want, rtol=0.0, atol=1e-13)
+            assert np.all(imp[b, L[b]:] == 0.0)
+
+
+def test_head_importance_mass_and_equal_keys():
+    """Each (head, token) distribution sums to one over the L committed keys;
+    with all keys of a kv-head equal it is uniform, 1/L per key."""
+    q, k, L = _importance_case(3)
+    heads = [0, 5, 7]
+    T = q.shape[1]
+    imp = oracle.head_importance(q, k, L, heads, 0.4)
+    for b in range(len(L)):
+        assert abs(imp[b].sum() - len(heads) * T) < 1e-11
+        assert np.all(imp[b, L[b]:] == 0.0)
+    flat = k.copy()
+    flat[:, :, :, :] = k[:, :1, :, :]  # every row equals row 0
+    imp = oracle.head_importance(q, flat, L, heads, 0.4)
+    for b in range(len(L)):
+        assert np.allclose(imp[b, : L[b]], len(heads) * T / L[b], rtol=1e-13, atol=0.0)
+
+
+def test_head_importance_follows_the_prefix_rows_only():
+    """Permuting the committed rows permutes the importances; the rows after
+    the prefix (draft slots) do not enter."""
+    q, k, L = _importance_case(5)
+    heads = [2, 4]
+    imp = oracle.head_importance(q, k, L, heads, 0.5)
+    rng = np.random.default_rng(9)
+    k2 = k.copy()
+    perms = []
+    for b in range(len(L)):
+        p = rng.permutation(int(L[b]))
+        perms.append(p)
+        k2[b, : L[b]] = k[b, p]
+        k2[b, L[b]:] = k[b, L[b]:] ^ np.uint16(0x1234)  # draft and spare rows changed
+    imp2 = oracle.head_importance(q, k2, L, heads, 0.5)
+    for b in range(len(L)):
+        assert np.allclose(imp2[b, : L[b]], imp[b, perms[b]], rtol=0.0, atol=1e-12)
+        assert np.all(imp2[b, L[b]:] == 0.0)
