@@ -258,6 +258,53 @@ def measure_next_rows(va, peak, steps=1024):
     return res
 
 
+def measure_scoring(va, peak, steps=256):
+    """The importance pass of a few query heads at the sparse workload's shape
+    (B16, T5, Hq32/Hkv8, prefixes 16K-32K, two synthetic retrieval heads on
+    kv-heads 2 and 5).  Device time per call from CUDA events around graphs
+    of 16 calls; the algorithmic bytes are the K rows of the listed kv-heads
+    (read once), the q rows and the importance rows written (Hkv per position).
+    The K rows of one call (about 200 MB) exceed the L2."""
+    w = W.make_workload("sparse", seed=0)
+    heads = list(w.score_heads)
+    group = w.Hq // w.Hkv
+    n_kv = len({h // group for h in heads})
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+    q, k, seqlens = w.q.cuda(), w.k_cache.cuda(), i32(w.seqlens)
+    score = torch.empty(w.B, w.Hkv, w.max_cache_len, dtype=torch.float32, device="cuda")
+    scratch = va.ScoreScratch(w.B, w.T, len(heads), w.max_cache_len)
+    total_L = int(w.seqlens.astype(np.int64).sum())
+    nbytes = total_L * n_kv * w.D * 2 + w.B * w.T * len(heads) * w.D * 2 + total_L * w.Hkv * 4
+
+    def fn():
+        va.verify_head_importance(q, k, seqlens, heads, score=score, scale=w.scale, scratch=scratch)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(16):
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // 16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * 16)
+    return {"workload": f"sparse shape: B{w.B} T{w.T} Hq{w.Hq} Hkv{w.Hkv} d{w.D} bf16, prefixes "
+                        f"16K-32K, heads {heads}",
+            "us_per_call": round(t * 1e6, 3), "algorithmic_bytes": nbytes,
+            "GBps": round(nbytes / t / 1e9, 1), "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
+            "launches_per_call": 2}
+
+
 def e2e_measure(w, va, steps):
     """Through the public API with host buffers: per step H2D the new inputs from
     pinned memory, run the call, D2H out and lse, and wait for them."""
@@ -443,6 +490,20 @@ def run_profile(args):
         va.verify_attn_check_status(ws)
         print(json.dumps({"profile": "after", "calls": args.calls, "status": "ok"}))
         return 0
+    if args.profile == "score":
+        w = W.make_workload("sparse", seed=0)
+        q, k = w.q.cuda(), w.k_cache.cuda()
+        seqlens = torch.from_numpy(w.seqlens).cuda()
+        score = torch.empty(w.B, w.Hkv, w.max_cache_len, dtype=torch.float32, device="cuda")
+        scratch = va.ScoreScratch(w.B, w.T, len(w.score_heads), w.max_cache_len)
+        ws = va.Workspace(256)
+        for _ in range(args.calls):
+            va.verify_head_importance(q, k, seqlens, list(w.score_heads), score=score, scale=w.scale,
+                                      scratch=scratch, workspace=ws)
+        torch.cuda.synchronize()
+        va.verify_attn_check_status(ws)
+        print(json.dumps({"profile": "score", "calls": args.calls, "status": "ok"}))
+        return 0
     case = DeviceCase(W.make_workload(args.profile, seed=0), va)
     for _ in range(args.calls):
         case.step()
@@ -576,9 +637,10 @@ def main():
     ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after"], default=None,
+    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after", "score"], default=None,
                     help="run --calls plain verification steps of one workload (for ncu) and exit; "
-                         "'after': --calls acceptance + KV commit pairs at the paged shape")
+                         "'after': --calls acceptance + KV commit pairs at the paged shape; "
+                         "'score': --calls importance passes at the sparse shape")
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -605,6 +667,7 @@ def main():
                             "us_per_step": round(r["dt"] * 1e6, 2), "tokens_per_s": round(r["tok_s"] / world, 1),
                             "call_us": round(r["call_s"] * 1e6, 2)}
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
+    scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -648,6 +711,8 @@ def main():
         line["other_configs"] = others
     if next_rows is not None:
         line["after_verification"] = next_rows
+    if scoring is not None:
+        line["scoring_pass"] = scoring
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -223,6 +223,39 @@ va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float
                              void *workspace, va_stream stream);
 
 /*
+ * Importance of the committed positions from a few query heads, the signal
+ * that feeds verify_build_index (Dustin section 1: the target model's
+ * attention scores are one signal of the global importance map; section 2:
+ * the estimate is computed on a few semantic retrieval heads only).  For
+ * sequence b with L = seqlens[b], every listed query head h and every token
+ * t < T of q, p[h,t] is the attention distribution of q[b][t][h] over the L
+ * committed keys of kv-head h / (Hq/Hkv) (score scale shape->scale; the rows
+ * after the prefix take no part), and
+ *   score[b][g][j] = sum over the listed heads and the T tokens of p[h,t][j]
+ * for j < L and every kv-head g: one map per sequence, repeated in each
+ * kv-head row so that verify_build_index takes it unchanged.  Entries
+ * j >= L are not written.
+ *   shape: B, T (<= 64), Hq, Hkv, scale; bf16 with D = 128 only.
+ *   q [B][T][Hq][128] and k_cache [B][max_cache_len][Hkv][128] bf16, 16-byte
+ *     aligned; seqlens [B] int32 (L <= max_cache_len and L <= score_stride,
+ *     device-checked: a bad value is recorded and clamped).
+ *   heads: HOST array of n_heads query-head indices in [0, Hq), 1 <= n_heads
+ *     <= 32, n_heads * T <= 256; a head listed twice counts twice.
+ *   score fp32 [B][Hkv][score_stride], 4-byte aligned.
+ *   scratch: caller-owned device memory of at least
+ *     verify_head_importance_scratch_size() bytes, 256-byte aligned (scores
+ *     of the listed heads and per-chunk partial sums; contents not kept).
+ *   workspace (may be NULL) receives device-side errors.
+ * Two kernels on `stream`; calls that share a scratch buffer must not overlap.
+ */
+size_t verify_head_importance_scratch_size(int B, int T, int n_heads, int max_cache_len);
+
+va_status verify_head_importance(const va_shape *shape, const void *q, const void *k_cache,
+                                 int max_cache_len, const int32_t *seqlens, const int32_t *heads,
+                                 int n_heads, float *score, int score_stride, void *scratch,
+                                 size_t scratch_bytes, void *workspace, va_stream stream);
+
+/*
  * After verification (Dustin section 1, step 5: accepted tokens join the
  * cache, rejected ones are dropped; HiSpec section 2: the entries of rejected
  * tokens are removed before the next phase, and the output equals the target

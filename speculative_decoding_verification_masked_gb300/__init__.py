@@ -4,6 +4,7 @@ The compute lives in libverify_attn.so (hand-written sm_103a CUDA, C ABI in
 include/verify_attn.h); this package builds it in-tree and binds it.
 """
 from .api import (  # noqa: F401
+    ScoreScratch,
     VerifyAttnError,
     Workspace,
     make_shape,
@@ -16,6 +17,7 @@ from .api import (  # noqa: F401
     verify_build_index,
     verify_commit_kv_dense,
     verify_commit_kv_paged,
+    verify_head_importance,
     verify_tree_mask_from_parents,
     version,
     workspace_size,

@@ -55,6 +55,8 @@ _SIGS = {
     "verify_accept_greedy": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "verify_commit_kv_dense": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "verify_commit_kv_paged": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "verify_head_importance_scratch_size": (_SZ, [_I, _I, _I, _I]),
+    "verify_head_importance": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, _I, _P, _I, _P, _SZ, _P, _P]),
     "verify_attn_check_status": (_I, [_P, _P]),
     "verify_attn_last_error": (ctypes.c_char_p, []),
     "verify_attn_version": (ctypes.c_char_p, []),
@@ -301,6 +303,44 @@ def verify_commit_kv_paged(k_pages, v_pages, page_table, seqlens, path, n_accept
                                         max_pages, _ptr(seqlens), _ptr(path), _ptr(n_accept), _ptr(seqlens_out),
                                         workspace.ptr if workspace is not None else None, _stream(stream)))
     return seqlens_out
+
+
+class ScoreScratch:
+    """Caller-owned device scratch of the scoring pass (256-byte aligned)."""
+
+    def __init__(self, B, T, n_heads, max_cache_len, device=None):
+        n = int(lib().verify_head_importance_scratch_size(int(B), int(T), int(n_heads), int(max_cache_len)))
+        if n == 0:
+            _check(VA_ERR_INVALID_ARG)
+        self.buffer = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+        self.offset = (-self.buffer.data_ptr()) % 256
+        self.nbytes = n
+
+    @property
+    def ptr(self) -> int:
+        return self.buffer.data_ptr() + self.offset
+
+
+def verify_head_importance(q, k_cache, seqlens, heads, score=None, score_stride=None, scale=None,
+                           scratch: ScoreScratch = None, workspace: Workspace = None, stream=None):
+    """Importance map of the committed positions from the listed query heads:
+    returns score fp32 [B][Hkv][score_stride] (entries past each L_b untouched;
+    a new tensor is zero-filled there)."""
+    B, T, Hq, D = q.shape
+    _, cap, Hkv, _ = k_cache.shape
+    heads = [int(h) for h in heads]
+    if score is None:
+        score = torch.zeros(B, Hkv, score_stride or cap, dtype=torch.float32, device=q.device)
+    stride = score.shape[-1]
+    if scratch is None:
+        scratch = ScoreScratch(B, T, len(heads), cap, device=q.device)
+    shape = make_shape(B, T, Hq, Hkv, D, _dtype_code(q), scale)
+    harr = (ctypes.c_int32 * len(heads))(*heads)
+    _check(lib().verify_head_importance(ctypes.byref(shape), _ptr(q), _ptr(k_cache), cap, _ptr(seqlens),
+                                        ctypes.cast(harr, ctypes.c_void_p), len(heads), _ptr(score), stride,
+                                        scratch.ptr, scratch.nbytes,
+                                        workspace.ptr if workspace is not None else None, _stream(stream)))
+    return score
 
 
 def verify_attn_check_status(workspace: Workspace, stream=None):

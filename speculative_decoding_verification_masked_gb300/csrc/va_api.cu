@@ -15,6 +15,7 @@
 #include "va_common.cuh"
 #include "va_kernels.h"
 #include "va_commit.h"
+#include "va_score.h"
 #include "verify_attn_testing.h"
 
 namespace {
@@ -477,6 +478,98 @@ va_status verify_commit_kv_dense(const va_shape *shape, void *k_cache, void *v_c
   cp.len_cap = max_cache_len;
   cudaError_t e = va::launch_commit_kv(cp, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  return ok();
+}
+
+size_t verify_head_importance_scratch_size(int B, int T, int n_heads, int max_cache_len) {
+  if (B < 1 || T < 1 || n_heads < 1 || max_cache_len < 1) return 0;
+  return va::score_scratch_bytes(B, n_heads * T, max_cache_len);
+}
+
+va_status verify_head_importance(const va_shape *shape, const void *q, const void *k_cache, int max_cache_len,
+                                 const int32_t *seqlens, const int32_t *heads, int n_heads, float *score,
+                                 int score_stride, void *scratch, size_t scratch_bytes, void *workspace,
+                                 va_stream stream) {
+  if (shape == nullptr) return fail(VA_ERR_INVALID_ARG, "shape is NULL");
+  const va_shape &s = *shape;
+  if (s.B < 1 || s.T < 1 || s.Hq < 1 || s.Hkv < 1 || s.Hq % s.Hkv != 0)
+    return fail(VA_ERR_INVALID_ARG, "bad shape (B=%d T=%d Hq=%d Hkv=%d)", s.B, s.T, s.Hq, s.Hkv);
+  if (!(s.scale > 0.f) || !isfinite(s.scale)) return fail(VA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (s.dtype != VA_DTYPE_BF16 || s.D != 128)
+    return fail(VA_ERR_UNSUPPORTED, "the scoring pass supports bf16 with D = 128");
+  if (s.T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d; at most 64 tokens are supported", s.T);
+  if (s.B > 65535) return fail(VA_ERR_UNSUPPORTED, "B=%d; at most 65535 sequences", s.B);
+  if (heads == nullptr || n_heads < 1) return fail(VA_ERR_INVALID_ARG, "list at least one query head");
+  if (n_heads > va::kScoreMaxHeads || n_heads * s.T > va::kScoreMaxRows)
+    return fail(VA_ERR_UNSUPPORTED, "n_heads=%d x T=%d: at most %d heads and %d rows", n_heads, s.T,
+                va::kScoreMaxHeads, va::kScoreMaxRows);
+  for (int i = 0; i < n_heads; ++i)
+    if (heads[i] < 0 || heads[i] >= s.Hq) return fail(VA_ERR_INVALID_ARG, "heads[%d]=%d is not in [0, Hq)", i, heads[i]);
+  if (q == nullptr || k_cache == nullptr || seqlens == nullptr || score == nullptr || scratch == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "q, k_cache, seqlens, score and scratch must not be NULL");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(score, 4))
+    return fail(VA_ERR_INVALID_ARG, "q and k_cache must be 16-byte aligned, score 4-byte aligned");
+  if (max_cache_len < 1 || score_stride < 1)
+    return fail(VA_ERR_INVALID_ARG, "max_cache_len and score_stride must be >= 1");
+  if (max_cache_len > (1 << 30)) return fail(VA_ERR_UNSUPPORTED, "max_cache_len above 2^30");
+  if (!aligned(scratch, 256)) return fail(VA_ERR_WORKSPACE, "scratch must be 256-byte aligned");
+  const size_t need = va::score_scratch_bytes(s.B, n_heads * s.T, max_cache_len);
+  if (scratch_bytes < need) return fail(VA_ERR_WORKSPACE, "scratch has %zu bytes, %zu needed", scratch_bytes, need);
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+
+  va::ScoreParams p;
+  memset(&p, 0, sizeof p);
+  p.B = s.B;
+  p.T = s.T;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.max_cache_len = max_cache_len;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k = static_cast<const __nv_bfloat16 *>(k_cache);
+  p.seqlens = seqlens;
+  p.R = n_heads * s.T;
+  p.n_chunks = (max_cache_len + va::kScoreChunk - 1) / va::kScoreChunk;
+  p.lpad = p.n_chunks * va::kScoreChunk;
+  p.logits = static_cast<float *>(scratch);
+  p.part = reinterpret_cast<float2 *>(static_cast<uint8_t *>(scratch) +
+                                      va::align256(sizeof(float) * (size_t)s.B * p.R * p.lpad));
+  p.score = score;
+  p.score_stride = score_stride;
+  p.score_vec4 = aligned(score, 16) && score_stride % 4 == 0;
+  p.status = static_cast<int *>(workspace);
+  // rows grouped by kv-head (a stable order of the listed heads), T rows per
+  // head; a unit is at most kScoreUnitRows consecutive rows of one kv-head
+  const int group = s.Hq / s.Hkv;
+  int order[va::kScoreMaxHeads];
+  for (int i = 0; i < n_heads; ++i) order[i] = i;
+  for (int i = 1; i < n_heads; ++i)  // insertion sort by kv-head, stable
+    for (int j = i; j > 0 && heads[order[j - 1]] / group > heads[order[j]] / group; --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  int r = 0;
+  for (int i = 0; i < n_heads; ++i)
+    for (int t = 0; t < s.T; ++t, ++r) {
+      p.row_head[r] = (int16_t)heads[order[i]];
+      p.row_t[r] = (int8_t)t;
+    }
+  int nu = 0;
+  for (int r0 = 0; r0 < p.R;) {
+    const int kvh = p.row_head[r0] / group;
+    int n = 0;
+    while (r0 + n < p.R && n < va::kScoreUnitRows && p.row_head[r0 + n] / group == kvh) ++n;
+    if (nu == va::kScoreMaxUnits) return fail(VA_ERR_UNSUPPORTED, "too many (kv-head, row block) units");
+    p.unit_kvh[nu] = (int16_t)kvh;
+    p.unit_row0[nu] = (int16_t)r0;
+    p.unit_n[nu] = (int8_t)n;
+    ++nu;
+    r0 += n;
+  }
+  p.n_units = nu;
+  cudaError_t e = va::launch_head_importance(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scoring launch");
   return ok();
 }
 

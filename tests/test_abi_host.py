@@ -118,3 +118,33 @@ def test_acceptance_and_commit_argument_checks():
         api.VA_ERR_INVALID_ARG  # page size not a power of two
     assert paged(ctypes.byref(s), FAKE, FAKE, 10, 16, None, 4, FAKE, FAKE, FAKE, None, None, None) == \
         api.VA_ERR_INVALID_ARG  # no page table
+
+
+def test_head_importance_argument_checks():
+    """The scoring pass rejects bad shapes, head lists and buffers on the host."""
+    L = api.lib()
+    f = L.verify_head_importance
+
+    def call(shape=None, heads=(3, 17), q=FAKE, scratch=FAKE, nbytes=1 << 30, max_len=100, stride=100, ws=None):
+        s = shape or _shape(T=5)
+        harr = (ctypes.c_int32 * max(1, len(heads)))(*heads)
+        return f(ctypes.byref(s), q, FAKE, max_len, FAKE, ctypes.cast(harr, ctypes.c_void_p), len(heads), FAKE,
+                 stride, scratch, nbytes, ws, None)
+
+    assert call(heads=(3, 32)) == api.VA_ERR_INVALID_ARG        # head out of range
+    assert call(heads=()) == api.VA_ERR_INVALID_ARG             # empty list
+    assert call(heads=tuple(range(33))) == api.VA_ERR_UNSUPPORTED  # more than 32 heads
+    assert call(shape=_shape(T=64), heads=(0, 1, 2, 3, 4)) == api.VA_ERR_UNSUPPORTED  # 320 rows
+    assert call(shape=_shape(T=5, D=64)) == api.VA_ERR_UNSUPPORTED
+    assert call(shape=_shape(T=5, dtype=2, D=64)) == api.VA_ERR_UNSUPPORTED
+    assert call(shape=_shape(T=5, Hq=30)) == api.VA_ERR_INVALID_ARG
+    assert call(q=None) == api.VA_ERR_INVALID_ARG
+    assert call(q=FAKE + 8) == api.VA_ERR_INVALID_ARG
+    assert call(scratch=FAKE + 16) == api.VA_ERR_WORKSPACE
+    assert call(nbytes=1024) == api.VA_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == api.VA_ERR_WORKSPACE
+    assert call(stride=0) == api.VA_ERR_INVALID_ARG
+    need = L.verify_head_importance_scratch_size(16, 5, 2, 32773)
+    chunks = (32773 + 255) // 256
+    assert need == 16 * 10 * chunks * 256 * 4 + (-(-16 * chunks * 10 * 8 // 256)) * 256
+    assert L.verify_head_importance_scratch_size(0, 5, 2, 100) == 0

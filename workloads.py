@@ -18,7 +18,9 @@ Workloads follow the shapes of the five measured configurations:
   depth 6, dense cache.
 * ``sparse`` -- B16, Hq32, Hkv8, d128, bf16, prefixes uniform in
   [16384, 32768], 5-token chain, per-(sequence, kv-head) verify set of 4 sinks,
-  256 recent tokens and top-scored rest (2048 in all), dense cache.
+  256 recent tokens and top-scored rest (2048 in all), dense cache; query
+  heads 9 and 22 (kv-heads 2 and 5) stand in for the profiled retrieval heads
+  of the importance pass.
 * ``paged``  -- B64, Hq32, Hkv8, d128, bf16, prefixes uniform in [2048, 8192],
   16-token pages behind a random page table, 16 draft tokens under a
   block mask (bidirectional inside 4-token blocks, causal across blocks).
@@ -203,6 +205,7 @@ class Workload:
     window: int = 0
     m_draft: int = 0
     budget: int = 0
+    score_heads: tuple = ()  # query heads of the importance pass (synthetic retrieval heads)
 
     @property
     def group(self) -> int:
@@ -256,7 +259,7 @@ def make_workload(name: str, seed: int = 0, **over) -> Workload:
         "chain": dict(layout="dense", B=1, T=8, Hq=32, Hkv=8, D=128, dtype="bf16", L=32768, tree="chain"),
         "tree": dict(layout="dense", B=1, T=64, Hq=32, Hkv=8, D=128, dtype="bf16", L=131072, tree="depth", depth=6),
         "sparse": dict(layout="sparse", B=16, T=5, Hq=32, Hkv=8, D=128, dtype="bf16", L_lo=16384, L_hi=32768,
-                       tree="chain", n_sink=4, window=256, budget=2048, m_draft=894),
+                       tree="chain", n_sink=4, window=256, budget=2048, m_draft=894, score_heads=(9, 22)),
         "paged": dict(layout="paged", B=64, T=16, Hq=32, Hkv=8, D=128, dtype="bf16", L_lo=2048, L_hi=8192,
                       tree="block", page_size=16),
     }
@@ -342,6 +345,7 @@ def make_workload(name: str, seed: int = 0, **over) -> Workload:
         w.window = int(p["window"])
         w.budget = int(p["budget"])
         w.m_draft = int(p["m_draft"])
+        w.score_heads = tuple(int(h) for h in p.get("score_heads", ()))
     return w
 
 
