@@ -11,14 +11,17 @@
 // builder takes it unchanged.
 //
 // Two launches:
-//  * head_logits_kernel -- one CTA per (256-key chunk, sequence).  Each warp
-//    scores its 32 keys against every unit (<= 8 query rows of one kv-head)
-//    on the tensor cores: S^T = K Q^T by mma.sync m16n8k16 with 16 keys on
-//    the M side, the unit's rows on N and the head dimension as K.  Every K
-//    row of the listed kv-heads is read once from HBM (streaming loads).  The
-//    scores (base-2 units) go to scratch, and per chunk and row the maximum
-//    and the sum of 2^(s - max).
-//  * head_score_kernel -- one CTA per (1024-key chunk, sequence): merges the
+//  * head_logits_kernel -- one 4-warp CTA per (128-key chunk, sequence,
+//    unit); a unit is up to 8 query rows of one kv-head.  Six CTAs share an
+//    SM (80 registers a thread), so that enough K rows are in flight to keep
+//    HBM busy without a shared-memory stage.  Each warp scores its 32
+//    keys against the unit's rows on the tensor cores: S^T = K Q^T by
+//    mma.sync m16n8k16 with 16 keys on the M side, the unit's rows on N and
+//    the head dimension as K.  Every K row of the listed kv-heads is read
+//    once from HBM (streaming loads).  The scores (base-2 units) go to
+//    scratch, and per chunk and row the maximum and the sum of 2^(s - max).
+//  * head_score_kernel -- one CTA per (1024-key chunk, sequence), chained by
+//    programmatic dependent launch: loads the first rows' scores, merges the
 //    chunk partials of every row into its log-sum-exp, then sums
 //    2^(s - lse) over the rows for four keys per thread and writes the sums
 //    to the Hkv rows of the output.
@@ -56,8 +59,8 @@ __device__ __forceinline__ uint32_t word(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-__global__ void __launch_bounds__(256) head_logits_kernel(const ScoreParams p) {
-  __shared__ float2 wpart[8][kScoreUnitRows];
+__global__ void __launch_bounds__(128, 6) head_logits_kernel(const ScoreParams p) {
+  __shared__ float2 wpart[4][kScoreUnitRows];
   const int c = blockIdx.x, b = blockIdx.y;
   const int L = score_len(p, b, c == 0 && threadIdx.x == 0);
   const int k0 = c * kScoreChunk;
@@ -65,103 +68,103 @@ __global__ void __launch_bounds__(256) head_logits_kernel(const ScoreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, qd = lane & 3;
   const int kb = k0 + warp * 32;
-
-  for (int u = 0; u < p.n_units; ++u) {
-    const int kvh = p.unit_kvh[u], row0 = p.unit_row0[u], nrow = p.unit_n[u];
-    // B operand: query row g of the unit at dims 8 qd + 32 j .. +7
-    uint4 wq[4];
-    if (g < nrow) {
-      const int r = row0 + g;
-      const uint4 *qr = reinterpret_cast<const uint4 *>(
-                            p.q + (((size_t)b * p.T + p.row_t[r]) * p.Hq + p.row_head[r]) * 128) + qd;
+  // the reduction grid may be scheduled once every CTA here has started
+  // (it waits for this grid's completion before reading anything)
+  pdl_launch_dependents();
+  const int u = blockIdx.z;
+  const int kvh = p.unit_kvh[u], row0 = p.unit_row0[u], nrow = p.unit_n[u];
+  // B operand: query row g of the unit at dims 8 qd + 32 j .. +7
+  uint4 wq[4];
+  if (g < nrow) {
+    const int r = row0 + g;
+    const uint4 *qr = reinterpret_cast<const uint4 *>(
+                          p.q + (((size_t)b * p.T + p.row_t[r]) * p.Hq + p.row_head[r]) * 128) + qd;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) wq[j] = __ldg(qr + 4 * j);
-    } else {
+    for (int j = 0; j < 4; ++j) wq[j] = __ldg(qr + 4 * j);
+  } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) wq[j] = make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) wq[j] = make_uint4(0, 0, 0, 0);
+  }
+  // A operand: keys kb + 16 s + 8 hf + g at the same dims (zero past L)
+  uint4 wk[2][2][4];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int key = kb + 16 * s + 8 * hf + g;
+      if (key < L) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(
+                              p.k + (((size_t)b * p.max_cache_len + key) * p.Hkv + kvh) * 128) + qd;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wk[s][hf][j] = __ldcs(kr + 4 * j);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wk[s][hf][j] = make_uint4(0, 0, 0, 0);
+      }
     }
-    // A operand: keys kb + 16 s + 8 hf + g at the same dims (zero past L)
-    uint4 wk[2][2][4];
+  }
+  float acc[2][4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
+  for (int s = 0; s < 2; ++s) {
+    acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int key = kb + 16 * s + 8 * hf + g;
-        if (key < L) {
-          const uint4 *kr = reinterpret_cast<const uint4 *>(
-                                p.k + (((size_t)b * p.max_cache_len + key) * p.Hkv + kvh) * 128) + qd;
+    for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) wk[s][hf][j] = __ldcs(kr + 4 * j);
-        } else {
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t a[4] = {word(wk[s][0][j], 2 * h2), word(wk[s][1][j], 2 * h2),
+                               word(wk[s][0][j], 2 * h2 + 1), word(wk[s][1][j], 2 * h2 + 1)};
+        mma_bf16(acc[s], a, word(wq[j], 2 * h2), word(wq[j], 2 * h2 + 1));
+      }
+    }
+  }
+  // acc[s][2 hf + e] = score of key kb + 16 s + 8 hf + g against unit row 2 qd + e
+  float x[2][4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) wk[s][hf][j] = make_uint4(0, 0, 0, 0);
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = kb + 16 * s + 8 * (i >> 1) + g;
+      x[s][i] = key < L ? acc[s][i] * p.scale_log2 : -INFINITY;
+    }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int rl = 2 * qd + e;
+    if (rl < nrow) {
+      float *lr = p.logits + ((size_t)b * p.R + row0 + rl) * p.lpad;
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int key = kb + 16 * s + 8 * hf + g;
+          if (key < L) lr[key] = x[s][2 * hf + e];
         }
-      }
     }
-    float acc[2][4];
+    // maximum and sum of 2^(s - max) of row rl over the warp's 32 keys
+    // (lanes with the same qd hold the same two rows)
+    float m = fmaxf(fmaxf(x[0][e], x[0][2 + e]), fmaxf(x[1][e], x[1][2 + e]));
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+    for (int off = 4; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float sum = 0.f;
+    if (m != -INFINITY)
+      sum = (ex2_approx(x[0][e] - m) + ex2_approx(x[0][2 + e] - m)) +
+            (ex2_approx(x[1][e] - m) + ex2_approx(x[1][2 + e] - m));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+    for (int off = 4; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (g == 0) wpart[warp][rl] = make_float2(m, sum);
+  }
+  __syncthreads();
+  if (threadIdx.x < nrow) {
+    const int rl = threadIdx.x;
+    float M = -INFINITY;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t a[4] = {word(wk[s][0][j], 2 * h2), word(wk[s][1][j], 2 * h2),
-                                 word(wk[s][0][j], 2 * h2 + 1), word(wk[s][1][j], 2 * h2 + 1)};
-          mma_bf16(acc[s], a, word(wq[j], 2 * h2), word(wq[j], 2 * h2 + 1));
-        }
-      }
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wpart[w][rl].x);
+    float S = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 v = wpart[w][rl];
+      if (v.x != -INFINITY) S += v.y * ex2_approx(v.x - M);
     }
-    // acc[s][2 hf + e] = score of key kb + 16 s + 8 hf + g against unit row 2 qd + e
-    float x[2][4];
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int key = kb + 16 * s + 8 * (i >> 1) + g;
-        x[s][i] = key < L ? acc[s][i] * p.scale_log2 : -INFINITY;
-      }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int rl = 2 * qd + e;
-      if (rl < nrow) {
-        float *lr = p.logits + ((size_t)b * p.R + row0 + rl) * p.lpad;
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int key = kb + 16 * s + 8 * hf + g;
-            if (key < L) lr[key] = x[s][2 * hf + e];
-          }
-      }
-      // maximum and sum of 2^(s - max) of row rl over the warp's 32 keys
-      // (lanes with the same qd hold the same two rows)
-      float m = fmaxf(fmaxf(x[0][e], x[0][2 + e]), fmaxf(x[1][e], x[1][2 + e]));
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float sum = 0.f;
-      if (m != -INFINITY)
-        sum = (ex2_approx(x[0][e] - m) + ex2_approx(x[0][2 + e] - m)) +
-              (ex2_approx(x[1][e] - m) + ex2_approx(x[1][2 + e] - m));
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (g == 0) wpart[warp][rl] = make_float2(m, sum);
-    }
-    __syncthreads();
-    if (threadIdx.x < nrow) {
-      const int rl = threadIdx.x;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) M = fmaxf(M, wpart[w][rl].x);
-      float S = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float2 v = wpart[w][rl];
-        if (v.x != -INFINITY) S += v.y * ex2_approx(v.x - M);
-      }
-      p.part[((size_t)b * p.n_chunks + c) * p.R + row0 + rl] = make_float2(M, S);
-    }
-    __syncthreads();
+    p.part[((size_t)b * p.n_chunks + c) * p.R + row0 + rl] = make_float2(M, S);
   }
 }
 
@@ -171,19 +174,36 @@ __global__ void __launch_bounds__(256) head_score_kernel(const ScoreParams p) {
   const int L = score_len(p, b, false);
   const int j0 = c * kScoreChunk2;
   if (j0 >= L) return;
+  pdl_wait_primary();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchk = (L + kScoreChunk - 1) / kScoreChunk;  // every one of these was written
+  const int j = j0 + 4 * threadIdx.x;
+  const bool act = j < L;
+  const float *lb = p.logits + (size_t)b * p.R * p.lpad + (act ? j : j0);
+  constexpr int PF = 8;  // rows whose scores are loaded while the partials are merged
+  float4 xs[PF];
+#pragma unroll
+  for (int i = 0; i < PF; ++i)
+    xs[i] = i < p.R ? __ldcg(reinterpret_cast<const float4 *>(lb + (size_t)i * p.lpad)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int nchk = (L + kScoreChunk - 1) / kScoreChunk;
   for (int r = warp; r < p.R; r += 8) {
     const float2 *pr = p.part + (size_t)b * p.n_chunks * p.R + r;
     float m = -INFINITY, s = 0.f;
-    for (int i = lane; i < nchk; i += 32) {
-      const float2 v = pr[(size_t)i * p.R];
-      if (v.x == -INFINITY) continue;
-      if (v.x > m) {
-        s = s * ex2_approx(m - v.x) + v.y;
-        m = v.x;
-      } else {
-        s += v.y * ex2_approx(v.x - m);
+    for (int i0 = lane; i0 < nchk; i0 += 128) {
+      float2 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + 32 * u;
+        v[u] = i < nchk ? __ldcg(pr + (size_t)i * p.R) : make_float2(-INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v[u].x == -INFINITY) continue;
+        if (v[u].x > m) {
+          s = s * ex2_approx(m - v[u].x) + v[u].y;
+          m = v[u].x;
+        } else {
+          s += v[u].y * ex2_approx(v[u].x - m);
+        }
       }
     }
 #pragma unroll
@@ -197,17 +217,34 @@ __global__ void __launch_bounds__(256) head_score_kernel(const ScoreParams p) {
     if (lane == 0) lse2[r] = m + log2f(s);
   }
   __syncthreads();
-  const int j = j0 + 4 * threadIdx.x;
-  if (j >= L) return;
+  if (!act) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float *lb = p.logits + (size_t)b * p.R * p.lpad + j;
-  for (int r = 0; r < p.R; ++r) {
-    const float4 x = __ldcg(reinterpret_cast<const float4 *>(lb + (size_t)r * p.lpad));
-    const float l = lse2[r];
-    acc.x += ex2_approx(x.x - l);
-    acc.y += ex2_approx(x.y - l);
-    acc.z += ex2_approx(x.z - l);
-    acc.w += ex2_approx(x.w - l);
+#pragma unroll
+  for (int i = 0; i < PF; ++i) {
+    if (i < p.R) {
+      const float l = lse2[i];
+      acc.x += ex2_approx(xs[i].x - l);
+      acc.y += ex2_approx(xs[i].y - l);
+      acc.z += ex2_approx(xs[i].z - l);
+      acc.w += ex2_approx(xs[i].w - l);
+    }
+  }
+  for (int r = PF; r < p.R; r += 4) {
+    float4 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      x[i] = r + i < p.R ? __ldcg(reinterpret_cast<const float4 *>(lb + (size_t)(r + i) * p.lpad))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (r + i < p.R) {
+        const float l = lse2[r + i];
+        acc.x += ex2_approx(x[i].x - l);
+        acc.y += ex2_approx(x[i].y - l);
+        acc.z += ex2_approx(x[i].z - l);
+        acc.w += ex2_approx(x[i].w - l);
+      }
+    }
   }
   const int n = min(4, L - j);
   for (int h = 0; h < p.Hkv; ++h) {
@@ -224,12 +261,20 @@ __global__ void __launch_bounds__(256) head_score_kernel(const ScoreParams p) {
 }
 
 cudaError_t launch_head_importance(const ScoreParams &p, cudaStream_t stream) {
-  head_logits_kernel<<<dim3((unsigned)p.n_chunks, (unsigned)p.B), 256, 0, stream>>>(p);
+  head_logits_kernel<<<dim3((unsigned)p.n_chunks, (unsigned)p.B, (unsigned)p.n_units), 128, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned n2 = (unsigned)((p.max_cache_len + kScoreChunk2 - 1) / kScoreChunk2);
-  head_score_kernel<<<dim3(n2, (unsigned)p.B), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n2, (unsigned)p.B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, head_score_kernel, p);
 }
 
 }  // namespace va

@@ -8,7 +8,7 @@
 
 namespace va {
 
-constexpr int kScoreChunk = 256;     // keys per CTA of the score pass (8 warps x 32 keys)
+constexpr int kScoreChunk = 128;     // keys per CTA of the score pass (4 warps x 32 keys)
 constexpr int kScoreChunk2 = 1024;   // keys per CTA of the reduction pass (256 threads x 4 keys)
 constexpr int kScoreUnitRows = 8;    // query rows of one kv-head per MMA unit (the N side)
 constexpr int kScoreMaxHeads = 32;   // listed query heads

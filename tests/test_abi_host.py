@@ -145,6 +145,6 @@ def test_head_importance_argument_checks():
     assert call(ws=FAKE + 16) == api.VA_ERR_WORKSPACE
     assert call(stride=0) == api.VA_ERR_INVALID_ARG
     need = L.verify_head_importance_scratch_size(16, 5, 2, 32773)
-    chunks = (32773 + 255) // 256
-    assert need == 16 * 10 * chunks * 256 * 4 + (-(-16 * chunks * 10 * 8 // 256)) * 256
+    chunks = (32773 + 127) // 128  # 128-key chunks of the score pass
+    assert need == 16 * 10 * chunks * 128 * 4 + (-(-16 * chunks * 10 * 8 // 256)) * 256
     assert L.verify_head_importance_scratch_size(0, 5, 2, 100) == 0
