@@ -472,6 +472,62 @@ def head_importance(q, k_cache, seqlens, heads, scale):
 
 
 # ----------------------------------------------------------------------------
+# rotary position embedding of the draft block (LongSpec section 1: the target
+# model keeps its own RoPE base; position ids may be arbitrary, e.g. the
+# anchor-offset indices 0, 1, 2, 3, 8192, 8193, ...)
+# ----------------------------------------------------------------------------
+
+def rope_rotate(x, positions, base):
+    """Rotary embedding of vectors x [..., D] at integer positions [...].
+
+    Reading (the pages name RoPE and its base, not the layout): the
+    rotate-half layout, pairing element i with element i + D/2 for
+    i < D/2, at the angle pos * base^(-2i/D):
+        out[i]       = x[i] cos(a_i) - x[i + D/2] sin(a_i)
+        out[i + D/2] = x[i + D/2] cos(a_i) + x[i] sin(a_i).
+    x: bf16 bits / fp32 / fp64; returns f64.
+    """
+    x = _widen(x)
+    D = x.shape[-1]
+    half = D // 2
+    inv_freq = float(base) ** (-(2.0 * np.arange(half)) / D)
+    ang = np.asarray(positions, dtype=np.float64)[..., None] * inv_freq
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rope_draft_dense(q, k_cache, seqlens, positions, base):
+    """q [B][T][Hq][D] rotated at positions[b][t] (every head), and the draft
+    key rows of a dense cache [B][Lmax][Hkv][D] -- slots L_b + t for t < T --
+    rotated at the same positions; the other cache rows are returned as they
+    are (widened).  Returns (q f64, k f64)."""
+    pos = np.asarray(positions)
+    qr = rope_rotate(q, pos[:, :, None], base)
+    k = _widen(k_cache).copy()
+    T = pos.shape[1]
+    for b in range(len(seqlens)):
+        L = int(seqlens[b])
+        k[b, L:L + T] = rope_rotate(k_cache[b, L:L + T], pos[b][:, None], base)
+    return qr, k
+
+
+def rope_draft_paged(q, k_pages, page_table, page_size, seqlens, positions, base):
+    """The same through a page table: the draft row of token t of sequence b
+    is row (L_b + t) % page_size of page page_table[b][(L_b + t) // page_size]."""
+    pos = np.asarray(positions)
+    qr = rope_rotate(q, pos[:, :, None], base)
+    k = _widen(k_pages).copy()
+    for b in range(len(seqlens)):
+        L = int(seqlens[b])
+        for t in range(pos.shape[1]):
+            slot = L + t
+            pg, row = int(page_table[b][slot // page_size]), slot % page_size
+            k[pg, row] = rope_rotate(k_pages[pg, row], pos[b, t], base)
+    return qr, k
+
+
+# ----------------------------------------------------------------------------
 # whole verification step for a workload object (duck-typed)
 # ----------------------------------------------------------------------------
 

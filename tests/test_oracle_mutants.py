@@ -116,6 +116,13 @@ PY_MUTANTS = {
     "importance_normalised_over_tokens": ("head_importance", "e / e.sum(axis=1, keepdims=True)",
                                           "e / e.sum(axis=0, keepdims=True)"),
     "importance_max_over_tokens": ("head_importance", "z.max(axis=1, keepdims=True)", "z.max(axis=0, keepdims=True)"),
+    "rope_sign": ("rope_rotate", "lo * c - hi * s", "lo * c + hi * s"),
+    "rope_interleaved_pairs": ("rope_rotate", "lo, hi = x[..., :half], x[..., half:]",
+                               "lo, hi = x[..., 0::2], x[..., 1::2]"),
+    "rope_frequency_exponent": ("rope_rotate", "(-(2.0 * np.arange(half)) / D)", "(-(1.0 * np.arange(half)) / D)"),
+    "rope_draft_slot": ("rope_draft_dense", "rope_rotate(k_cache[b, L:L + T], pos[b][:, None], base)",
+                        "rope_rotate(k_cache[b, L + 1:L + T + 1], pos[b][:, None], base)"),
+    "rope_paged_row": ("rope_draft_paged", "slot % page_size", "(slot + 1) % page_size"),
 }
 
 
@@ -134,6 +141,10 @@ def _py_pins_pass():
             pins.test_head_importance_matches_torch_softmax(seed)
         pins.test_head_importance_mass_and_equal_keys()
         pins.test_head_importance_follows_the_prefix_rows_only()
+        pins.test_rope_hand()
+        pins.test_rope_matches_complex_rotation(0)
+        pins.test_rope_invariants()
+        pins.test_rope_draft_rows_only()
         return True
     except (AssertionError, IndexError, ValueError):
         return False

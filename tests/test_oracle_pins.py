@@ -605,3 +605,83 @@ def test_head_importance_follows_the_prefix_rows_only():
     for b in range(len(L)):
         assert np.allclose(imp2[b, : L[b]], imp[b, perms[b]], rtol=0.0, atol=1e-12)
         assert np.all(imp2[b, L[b]:] == 0.0)
+
+
+# ----------------------------------------------------------------------------
+# rotary position embedding of the draft block
+# ----------------------------------------------------------------------------
+
+def test_rope_hand():
+    with open(os.path.join(GOLD, "rope_hand.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        out = oracle.rope_rotate(np.array(case["x"], np.float64), case["pos"], g["base"])
+        assert np.allclose(out, case["out"], rtol=0.0, atol=1e-15), case
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_rope_matches_complex_rotation(seed):
+    """Each pair (x_i, x_{i+D/2}) is the complex number x_i + i x_{i+D/2}
+    multiplied by exp(i pos theta_i), theta_i = base^(-2i/D) (numpy complex)."""
+    rng = np.random.default_rng(seed)
+    D, base = 128, 500000.0
+    x = rng.standard_normal((6, D))
+    pos = rng.integers(0, 140000, size=6)
+    z = (x[:, : D // 2] + 1j * x[:, D // 2:]) * np.exp(1j * pos[:, None] * base ** (-np.arange(0, D, 2) / D))
+    want = np.concatenate([z.real, z.imag], axis=1)
+    assert np.allclose(oracle.rope_rotate(x, pos, base), want, rtol=0.0, atol=1e-9)
+
+
+def test_rope_invariants():
+    """Rotations keep each pair's length, compose by adding positions, and make
+    q.k depend on the positions only through their difference."""
+    rng = np.random.default_rng(4)
+    D, base = 64, 10000.0
+    q, k = rng.standard_normal((2, D))
+    r = oracle.rope_rotate(q, 37, base)
+    h = D // 2
+    assert np.allclose(r[:h] ** 2 + r[h:] ** 2, q[:h] ** 2 + q[h:] ** 2, rtol=1e-12)
+    assert np.allclose(oracle.rope_rotate(r, 1000, base), oracle.rope_rotate(q, 1037, base), atol=1e-10)
+    d1 = oracle.rope_rotate(q, 500, base) @ oracle.rope_rotate(k, 480, base)
+    d2 = oracle.rope_rotate(q, 9020, base) @ oracle.rope_rotate(k, 9000, base)
+    assert abs(d1 - d2) < 1e-9
+    assert np.array_equal(oracle.rope_rotate(q, 0, base), q)
+
+
+def test_rope_draft_rows_only():
+    """Only the T draft rows after each prefix are rotated, each at its token's
+    position (a tree's positions: L_b + depth), and a paged cache gives the
+    same rows as the contiguous one."""
+    rng = np.random.default_rng(6)
+    B, T, Hq, Hkv, D, ps = 3, 5, 4, 2, 8, 4
+    L = np.array([6, 0, 11], np.int32)
+    cap = int(L.max()) + T + 2
+    q = rng.standard_normal((B, T, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((B, cap, Hkv, D)).astype(np.float32)
+    parent = np.stack([W.random_parents(T, rng) for _ in range(B)])
+    pos = L[:, None] + np.stack([W.chain_depths(p) for p in parent])
+    qr, kr = oracle.rope_draft_dense(q, k, L, pos, 10000.0)
+    for b in range(B):
+        for t in range(T):
+            assert np.allclose(qr[b, t], oracle.rope_rotate(q[b, t], pos[b, t], 10000.0), atol=0)
+            assert np.allclose(kr[b, L[b] + t], oracle.rope_rotate(k[b, L[b] + t], pos[b, t], 10000.0), atol=0)
+        keep = np.ones(cap, bool)
+        keep[L[b]:L[b] + T] = False
+        assert np.array_equal(kr[b, keep], k[b, keep].astype(np.float64))
+    # paged: the same sequences behind a shuffled page table
+    need = (L + T + ps - 1) // ps
+    P = int(need.sum()) + 1
+    perm = rng.permutation(P)
+    table = np.full((B, int(need.max())), -1, np.int32)
+    pages = rng.standard_normal((P, ps, Hkv, D)).astype(np.float32)
+    off = 0
+    for b in range(B):
+        table[b, : need[b]] = perm[off: off + need[b]]
+        off += need[b]
+    qp, kp = oracle.rope_draft_paged(q, pages, table, ps, L, pos, 10000.0)
+    assert np.array_equal(qp, qr)
+    for b in range(B):
+        n = int(L[b]) + T
+        dense = oracle.gather_pages(pages, table[b], n, ps)[None]
+        _, kd = oracle.rope_draft_dense(q[b:b + 1], dense, L[b:b + 1], pos[b:b + 1], 10000.0)
+        assert np.array_equal(oracle.gather_pages(kp, table[b], n, ps), kd[0])
