@@ -258,6 +258,49 @@ def measure_next_rows(va, peak, steps=1024):
     return res
 
 
+def measure_rope(va, peak, steps=1024):
+    """The rotary embedding of the draft block at the paged workload's shape
+    (B64, T16, Hq32/Hkv8, d128 bf16, 16-row pages, tree positions L + depth):
+    every head of q and the T draft key rows, read and written once.  Device
+    time per call from CUDA events around graphs of 64 calls (the rows are
+    rotated again each call; the traffic does not change)."""
+    w = W.make_workload("paged", seed=0, tree="random")
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+    depth = np.stack([W.chain_depths(p) for p in w.parent])
+    pos = i32(w.seqlens[:, None] + depth)
+    q, k, table, seqlens = w.q.cuda(), w.k_pages.cuda(), i32(w.page_table), i32(w.seqlens)
+    nbytes = 2 * w.B * w.T * (w.Hq + w.Hkv) * w.D * 2
+
+    def fn():
+        va.verify_rope_draft_paged(q, k, table, seqlens, pos, 500000.0)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(64):
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // 64)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / (reps * 64)
+    return {"workload": f"paged shape: B{w.B} T{w.T} Hq{w.Hq} Hkv{w.Hkv} d{w.D} bf16, 16-row pages, "
+                        "tree positions",
+            "us_per_call": round(t * 1e6, 3), "algorithmic_bytes": nbytes,
+            "GBps": round(nbytes / t / 1e9, 1), "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
+            "launches_per_call": 1,
+            "note": "about 21 MB a call: launch- and latency-bound, the rows mostly served from L2 in the loop"}
+
+
 def measure_scoring(va, peak, steps=256):
     """The importance pass of a few query heads at the sparse workload's shape
     (B16, T5, Hq32/Hkv8, prefixes 16K-32K, two synthetic retrieval heads on
@@ -490,6 +533,18 @@ def run_profile(args):
         va.verify_attn_check_status(ws)
         print(json.dumps({"profile": "after", "calls": args.calls, "status": "ok"}))
         return 0
+    if args.profile == "rope":
+        w = W.make_workload("paged", seed=0, tree="random")
+        depth = np.stack([W.chain_depths(p) for p in w.parent])
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+        q, k, ws = w.q.cuda(), w.k_pages.cuda(), va.Workspace(256)
+        for _ in range(args.calls):
+            va.verify_rope_draft_paged(q, k, i32(w.page_table), i32(w.seqlens), i32(w.seqlens[:, None] + depth),
+                                       500000.0, workspace=ws)
+        torch.cuda.synchronize()
+        va.verify_attn_check_status(ws)
+        print(json.dumps({"profile": "rope", "calls": args.calls, "status": "ok"}))
+        return 0
     if args.profile == "score":
         w = W.make_workload("sparse", seed=0)
         q, k = w.q.cuda(), w.k_cache.cuda()
@@ -637,10 +692,11 @@ def main():
     ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after", "score"], default=None,
+    ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after", "score", "rope"], default=None,
                     help="run --calls plain verification steps of one workload (for ncu) and exit; "
                          "'after': --calls acceptance + KV commit pairs at the paged shape; "
-                         "'score': --calls importance passes at the sparse shape")
+                         "'score': --calls importance passes at the sparse shape; "
+                         "'rope': --calls draft-block rotations at the paged shape")
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -668,6 +724,7 @@ def main():
                             "call_us": round(r["call_s"] * 1e6, 2)}
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
+    rope = measure_rope(va, peak) if args.all_configs and rank == 0 else None
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -713,6 +770,8 @@ def main():
         line["after_verification"] = next_rows
     if scoring is not None:
         line["scoring_pass"] = scoring
+    if rope is not None:
+        line["rope_draft"] = rope
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -32,7 +32,8 @@
  *   tree_parent  [B][T] int32         -1 for a root, else 0 <= parent[i] < i
  *   tree_mask    [B][T][W] uint32     W = ceil(T/32); bit j%32 of word j/32 of
  *                                     row i set = draft token i sees draft token j
- *   positions    [B][T] int32         reserved (see below)
+ *   positions    [B][T] int32         position id of draft token t (read only by
+ *                                     verify_rope_draft_*; see there)
  * Draft keys.  The T draft tokens' keys and values are already in the cache at
  *   logical slots L_b .. L_b+T-1 (append, then verify; rejected entries are
  *   dropped afterwards).
@@ -104,9 +105,9 @@ va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream
  * LongSpec section 2.C: unmasked split-KV pass over the L_b cached keys
  * (FlashAttention-style, no mask), masked pass over the T draft keys at slots
  * L_b..L_b+T-1, exact log-sum-exp merge.  Requires L_b + T <= max_cache_len
- * (checked on the device).  positions may be NULL; it is reserved for a fused
- * rotary embedding and is not read by this version (q and k must already
- * carry their positional rotation).
+ * (checked on the device).  positions may be NULL and is not read: q and k
+ * must already carry their positional rotation (verify_rope_draft_dense /
+ * _paged rotates q and the draft keys in one launch before this call).
  */
 va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_cache,
                             const void *v_cache, int max_cache_len, const int32_t *seqlens,
@@ -221,6 +222,41 @@ va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float
                              const float *score_target, int score_stride, int n_sink, int window,
                              int m_draft, int budget, int32_t *indices, int32_t *n_indices,
                              void *workspace, va_stream stream);
+
+/*
+ * Rotary position embedding of the draft block, in place (LongSpec section 1:
+ * the target model keeps its own RoPE base; position ids may be arbitrary,
+ * e.g. the anchor-offset ids 0, 1, 2, 3, 8192, 8193, ...).  For every
+ * sequence b and draft token t < T, with p = positions[b][t]:
+ *   every query head of q[b][t], and the key row of every kv-head at logical
+ *   slot L_b + t of the cache (L_b = seqlens[b]),
+ * are rotated pairwise in the rotate-half layout: element i pairs with
+ * element i + D/2 (i < D/2) at the angle p * rope_base^(-2i/D),
+ *   x'[i] = x[i] cos - x[i+D/2] sin,   x'[i+D/2] = x[i+D/2] cos + x[i] sin.
+ * Angles are formed and reduced in fp64, rows rotated in fp32 and rounded
+ * back to the element type.  Use: append the draft keys and values
+ * unrotated at slots L_b .. L_b+T-1, call this with the draft tokens'
+ * positions (L_b + depth for a tree, so an accepted path ends up rotated as
+ * a plain sequence after verify_commit_kv_*), then call verify_attn_*.  The
+ * value cache and every other key row are not touched.
+ *   shape: B, T (<= 64), Hq, Hkv (<= 256), D (even, <= 256), dtype bf16 or
+ *     fp32; scale is not used.
+ *   q [B][T][Hq][D], positions [B][T] int32 (any value), seqlens [B] int32.
+ *   Dense: k_cache [B][max_cache_len][Hkv][D], L_b + T <= max_cache_len.
+ *   Paged: k_pages [num_pages][page_size][Hkv][D] behind page_table as for
+ *     verify_attn_paged.
+ * A sequence whose L_b or page entries are out of range keeps its key rows
+ * unrotated (its q rows are still rotated) and VA_ERR_DEVICE_BOUNDS is
+ * recorded in `workspace` (may be NULL).
+ */
+va_status verify_rope_draft_dense(const va_shape *shape, void *q, void *k_cache, int max_cache_len,
+                                  const int32_t *seqlens, const int32_t *positions, float rope_base,
+                                  void *workspace, va_stream stream);
+
+va_status verify_rope_draft_paged(const va_shape *shape, void *q, void *k_pages, int num_pages,
+                                  int page_size, const int32_t *page_table, int max_pages_per_seq,
+                                  const int32_t *seqlens, const int32_t *positions, float rope_base,
+                                  void *workspace, va_stream stream);
 
 /*
  * Importance of the committed positions from a few query heads, the signal

@@ -18,6 +18,8 @@ from .api import (  # noqa: F401
     verify_commit_kv_dense,
     verify_commit_kv_paged,
     verify_head_importance,
+    verify_rope_draft_dense,
+    verify_rope_draft_paged,
     verify_tree_mask_from_parents,
     version,
     workspace_size,

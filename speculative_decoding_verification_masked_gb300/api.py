@@ -55,6 +55,9 @@ _SIGS = {
     "verify_accept_greedy": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "verify_commit_kv_dense": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "verify_commit_kv_paged": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "verify_rope_draft_dense": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, ctypes.c_float, _P, _P]),
+    "verify_rope_draft_paged": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _I, _P, _I, _P, _P, ctypes.c_float, _P,
+                                     _P]),
     "verify_head_importance_scratch_size": (_SZ, [_I, _I, _I, _I]),
     "verify_head_importance": (_I, [ctypes.POINTER(VaShape), _P, _P, _I, _P, _P, _I, _P, _I, _P, _SZ, _P, _P]),
     "verify_attn_check_status": (_I, [_P, _P]),
@@ -303,6 +306,29 @@ def verify_commit_kv_paged(k_pages, v_pages, page_table, seqlens, path, n_accept
                                         max_pages, _ptr(seqlens), _ptr(path), _ptr(n_accept), _ptr(seqlens_out),
                                         workspace.ptr if workspace is not None else None, _stream(stream)))
     return seqlens_out
+
+
+def verify_rope_draft_dense(q, k_cache, seqlens, positions, rope_base=10000.0, workspace: Workspace = None,
+                            stream=None):
+    """Rotate, in place, every head of q [B][T][Hq][D] and the draft key rows
+    (slots L_b .. L_b+T-1) of k_cache [B][len][Hkv][D] at positions [B][T]."""
+    B, T, Hq, D = q.shape
+    _, cap, Hkv, _ = k_cache.shape
+    shape = make_shape(B, T, Hq, Hkv, D, _dtype_code(q), 1.0)
+    _check(lib().verify_rope_draft_dense(ctypes.byref(shape), _ptr(q), _ptr(k_cache), cap, _ptr(seqlens),
+                                         _ptr(positions), float(rope_base),
+                                         workspace.ptr if workspace is not None else None, _stream(stream)))
+
+
+def verify_rope_draft_paged(q, k_pages, page_table, seqlens, positions, rope_base=10000.0,
+                            workspace: Workspace = None, stream=None):
+    """The same rotation through a page table; pages [P][page][Hkv][D]."""
+    B, T, Hq, D = q.shape
+    P, ps, Hkv, _ = k_pages.shape
+    shape = make_shape(B, T, Hq, Hkv, D, _dtype_code(q), 1.0)
+    _check(lib().verify_rope_draft_paged(ctypes.byref(shape), _ptr(q), _ptr(k_pages), P, ps, _ptr(page_table),
+                                         page_table.shape[1], _ptr(seqlens), _ptr(positions), float(rope_base),
+                                         workspace.ptr if workspace is not None else None, _stream(stream)))
 
 
 class ScoreScratch:

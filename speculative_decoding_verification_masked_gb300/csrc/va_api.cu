@@ -16,6 +16,7 @@
 #include "va_kernels.h"
 #include "va_commit.h"
 #include "va_score.h"
+#include "va_rope.h"
 #include "verify_attn_testing.h"
 
 namespace {
@@ -326,6 +327,39 @@ va_status commit_common(const va_shape *shape, void *k, void *v, const int32_t *
   cp.status = static_cast<int *>(workspace);
   return VA_OK;
 }
+
+va_status rope_common(const va_shape *shape, void *q, void *k, const int32_t *seqlens, const int32_t *positions,
+                      float rope_base, void *workspace, va::RopeParams &rp) {
+  if (shape == nullptr) return fail(VA_ERR_INVALID_ARG, "shape is NULL");
+  const va_shape &s = *shape;
+  if (s.B < 1 || s.T < 1 || s.Hq < 1 || s.Hkv < 1 || s.Hq % s.Hkv != 0)
+    return fail(VA_ERR_INVALID_ARG, "bad shape (B=%d T=%d Hq=%d Hkv=%d)", s.B, s.T, s.Hq, s.Hkv);
+  if (s.T > 64) return fail(VA_ERR_UNSUPPORTED, "T=%d; at most 64 draft tokens are supported", s.T);
+  if (s.B > 65535 || s.Hkv > 256) return fail(VA_ERR_UNSUPPORTED, "B <= 65535 and Hkv <= 256 are supported");
+  if (s.dtype != VA_DTYPE_BF16 && s.dtype != VA_DTYPE_FP32) return fail(VA_ERR_INVALID_ARG, "unknown dtype %d", (int)s.dtype);
+  if (s.D < 2 || s.D > 256 || s.D % 2 != 0) return fail(VA_ERR_UNSUPPORTED, "D=%d; an even D <= 256 is supported", s.D);
+  if (!(rope_base > 0.f) || !isfinite(rope_base)) return fail(VA_ERR_INVALID_ARG, "rope_base must be finite and > 0");
+  if (q == nullptr || k == nullptr || seqlens == nullptr || positions == nullptr)
+    return fail(VA_ERR_INVALID_ARG, "q, the key cache, seqlens and positions must not be NULL");
+  const size_t es = s.dtype == VA_DTYPE_BF16 ? 2 : 4;
+  if (!aligned(q, es) || !aligned(k, es)) return fail(VA_ERR_INVALID_ARG, "q and the key cache must be element-aligned");
+  if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  memset(&rp, 0, sizeof rp);
+  rp.B = s.B;
+  rp.T = s.T;
+  rp.Hq = s.Hq;
+  rp.Hkv = s.Hkv;
+  rp.D = s.D;
+  rp.fp32 = s.dtype == VA_DTYPE_FP32 ? 1 : 0;
+  rp.vec8 = s.D % 16 == 0 && aligned(q, 16) && aligned(k, 16) ? 1 : 0;
+  for (int i = 0; i < s.D / 2; ++i) rp.inv_freq[i] = pow((double)rope_base, -(double)(2 * i) / s.D);
+  rp.q = q;
+  rp.k = k;
+  rp.seqlens = seqlens;
+  rp.positions = positions;
+  rp.status = static_cast<int *>(workspace);
+  return VA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -570,6 +604,45 @@ va_status verify_head_importance(const va_shape *shape, const void *q, const voi
   p.n_units = nu;
   cudaError_t e = va::launch_head_importance(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "scoring launch");
+  return ok();
+}
+
+va_status verify_rope_draft_dense(const va_shape *shape, void *q, void *k_cache, int max_cache_len,
+                                  const int32_t *seqlens, const int32_t *positions, float rope_base,
+                                  void *workspace, va_stream stream) {
+  va::RopeParams rp;
+  va_status st = rope_common(shape, q, k_cache, seqlens, positions, rope_base, workspace, rp);
+  if (st != VA_OK) return st;
+  if (max_cache_len < shape->T)
+    return fail(VA_ERR_INVALID_ARG, "max_cache_len=%d is smaller than T=%d", max_cache_len, shape->T);
+  rp.len_cap = max_cache_len;
+  cudaError_t e = va::launch_rope_draft(rp, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+  return ok();
+}
+
+va_status verify_rope_draft_paged(const va_shape *shape, void *q, void *k_pages, int num_pages, int page_size,
+                                  const int32_t *page_table, int max_pages_per_seq, const int32_t *seqlens,
+                                  const int32_t *positions, float rope_base, void *workspace, va_stream stream) {
+  va::RopeParams rp;
+  va_status st = rope_common(shape, q, k_pages, seqlens, positions, rope_base, workspace, rp);
+  if (st != VA_OK) return st;
+  if (page_table == nullptr) return fail(VA_ERR_INVALID_ARG, "page_table must not be NULL");
+  if (page_size < 1 || page_size > 1024 || (page_size & (page_size - 1)) != 0)
+    return fail(VA_ERR_INVALID_ARG, "page_size=%d must be a power of two in [1, 1024]", page_size);
+  if (num_pages < 1 || max_pages_per_seq < 1) return fail(VA_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
+  const long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap < shape->T || cap >= (1ll << 31))
+    return fail(VA_ERR_INVALID_ARG, "max_pages_per_seq * page_size = %lld must be in [T, 2^31)", cap);
+  rp.len_cap = (int)cap;
+  rp.page_table = page_table;
+  rp.num_pages = num_pages;
+  rp.max_pages = max_pages_per_seq;
+  int shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  rp.page_shift = shift;
+  cudaError_t e = va::launch_rope_draft(rp, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope launch");
   return ok();
 }
 

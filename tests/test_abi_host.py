@@ -148,3 +148,23 @@ def test_head_importance_argument_checks():
     chunks = (32773 + 127) // 128  # 128-key chunks of the score pass
     assert need == 16 * 10 * chunks * 128 * 4 + (-(-16 * chunks * 10 * 8 // 256)) * 256
     assert L.verify_head_importance_scratch_size(0, 5, 2, 100) == 0
+
+
+def test_rope_argument_checks():
+    L = api.lib()
+    d = L.verify_rope_draft_dense
+    p = L.verify_rope_draft_paged
+    s = _shape(T=5)
+    assert d(None, FAKE, FAKE, 100, FAKE, FAKE, 10000.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), None, FAKE, 100, FAKE, FAKE, 10000.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), FAKE, FAKE, 100, FAKE, None, 10000.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), FAKE, FAKE, 100, FAKE, FAKE, 0.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), FAKE, FAKE, 100, FAKE, FAKE, float("inf"), None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), FAKE + 1, FAKE, 100, FAKE, FAKE, 10000.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(s), FAKE, FAKE, 4, FAKE, FAKE, 10000.0, None, None) == api.VA_ERR_INVALID_ARG
+    assert d(ctypes.byref(_shape(T=5, D=65)), FAKE, FAKE, 100, FAKE, FAKE, 1e4, None, None) == api.VA_ERR_UNSUPPORTED
+    assert d(ctypes.byref(_shape(T=5, D=258)), FAKE, FAKE, 100, FAKE, FAKE, 1e4, None, None) == api.VA_ERR_UNSUPPORTED
+    assert d(ctypes.byref(_shape(T=65)), FAKE, FAKE, 100, FAKE, FAKE, 1e4, None, None) == api.VA_ERR_UNSUPPORTED
+    assert d(ctypes.byref(s), FAKE, FAKE, 100, FAKE, FAKE, 1e4, FAKE + 16, None) == api.VA_ERR_WORKSPACE
+    assert p(ctypes.byref(s), FAKE, FAKE, 10, 12, FAKE, 4, FAKE, FAKE, 1e4, None, None) == api.VA_ERR_INVALID_ARG
+    assert p(ctypes.byref(s), FAKE, FAKE, 10, 16, None, 4, FAKE, FAKE, 1e4, None, None) == api.VA_ERR_INVALID_ARG
