@@ -668,8 +668,10 @@ def measure_config(name, va, args, want_e2e, want_cpu, rank, dist):
     gbs = whole_job_rate(bytes_step, dt, dist) / 1e9
     durs = per_call_durations(cases, 200)
     call_s = statistics.mean(durs)
+    call_pct = [float(x) for x in np.percentile(np.asarray(durs, dtype=np.float64), [10, 50, 90])]
     res = {"w": w, "dt": dt_max, "gbs": gbs, "tok_s": w.tokens() * world / dt_max, "call_s": call_s,
-           "call_gbs": bytes_step / call_s / 1e9, "clocks": clk, "n_copies": n_copies, "steps": steps_done}
+           "call_gbs": bytes_step / call_s / 1e9, "call_pct": call_pct, "clocks": clk, "n_copies": n_copies,
+           "steps": steps_done}
     if want_e2e:
         e_dt, h2d, d2h = e2e_measure(w, va, max(20, min(args.steps, 200)))
         e_dt = max_over_ranks(e_dt, dist)
@@ -721,7 +723,8 @@ def main():
             r = measure_config(name, va, args, want_e2e=False, want_cpu=False, rank=rank, dist=dist)
             others[name] = {"GBps": round(r["gbs"] / world, 1), "frac_of_measured_hbm": round(r["gbs"] / world / peak, 4),
                             "us_per_step": round(r["dt"] * 1e6, 2), "tokens_per_s": round(r["tok_s"] / world, 1),
-                            "call_us": round(r["call_s"] * 1e6, 2)}
+                            "call_us": round(r["call_s"] * 1e6, 2),
+                            "call_us_p10_p50_p90": [round(x * 1e6, 2) for x in r["call_pct"]]}
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
     rope = measure_rope(va, peak) if args.all_configs and rank == 0 else None
@@ -757,7 +760,9 @@ def main():
                      "frac": round(kern_gbs / peak, 4), "traffic": profiled_traffic(args.config),
                      "kernel": kernel_name, "kernel_us": round(kern_s * 1e6, 3),
                      "kernel_us_from": "timed region / steps" if launches == 1 else "single-call CUDA events",
-                     "call_us": round(main_res["call_s"] * 1e6, 3), "peak_kind": peak_kind},
+                     "call_us": round(main_res["call_s"] * 1e6, 3),
+                     "call_us_p10_p50_p90": [round(x * 1e6, 3) for x in main_res["call_pct"]],
+                     "peak_kind": peak_kind},
         "e2e": main_res.get("e2e"),
         "gpu_launches": main_res["steps"] * launches,
         "clocks": main_res["clocks"],
