@@ -6,7 +6,9 @@
   partials are all-gathered and merged by the LSE merge (LongSpec 2.C, the
   log-sum-exp fusion), which must equal the unsplit result.  The attention and
   the merge here are the oracle's; the device merge of gathered partials is
-  verify_attn_combine, covered by the GPU tests.
+  verify_attn_combine, covered by the GPU tests;
+* the importance pass split by position the same way: per-row (max, sum)
+  partials all-gathered, merged, and each rank's positions normalised.
 """
 import os
 import socket
@@ -72,7 +74,39 @@ def _context_parallel_merge(rank, world):
     np.testing.assert_allclose(lse_m.reshape(T, w.Hq).T, ref_lse, rtol=0, atol=1e-12)
 
 
-CASES = {"bench_replica_timing": _bench_replica_timing, "context_parallel_merge": _context_parallel_merge}
+def _context_parallel_importance(rank, world):
+    """The importance pass split by position: each rank scores its share of
+    one sequence's committed keys for the listed heads, keeps per-row
+    (maximum, sum of exp) partials, all-gathers those partials (the one
+    exchange step, 2 floats per row and rank), merges them into each row's
+    log-sum-exp and normalises its own positions; the shares concatenated are
+    the unsplit importance map."""
+    w = W.make_workload("sparse", seed=5, B=1, L_lo=300, L_hi=300, Hq=8, Hkv=2, D=16, T=3)
+    heads = [1, 6]
+    L = int(w.seqlens[0])
+    q = oracle._widen(W.bf16_bits(w.q))[0]            # [T][Hq][D]
+    k = oracle._widen(W.bf16_bits(w.k_cache))[0, :L]  # [L][Hkv][D]
+    group = w.Hq // w.Hkv
+    a, b = rank * L // world, (rank + 1) * L // world
+    z = np.stack([w.scale * (q[:, h] @ k[a:b, h // group].T) for h in heads])  # [heads][T][share]
+    m = z.max(axis=2)
+    part = torch.from_numpy(np.stack([m, np.exp(z - m[..., None]).sum(axis=2)], axis=-1))  # [heads][T][2]
+    gathered = [torch.empty_like(part) for _ in range(world)]
+    dist.all_gather(gathered, part)
+    g = torch.stack(gathered).numpy()  # [world][heads][T][2]
+    M = g[..., 0].max(axis=0)
+    lse = M + np.log((g[..., 1] * np.exp(g[..., 0] - M)).sum(axis=0))
+    mine = np.exp(z - lse[..., None]).sum(axis=(0, 1))  # this rank's positions
+    sizes = [(r + 1) * L // world - r * L // world for r in range(world)]
+    shares = [torch.empty(n, dtype=torch.float64) for n in sizes]
+    dist.all_gather(shares, torch.from_numpy(mine))
+    got = torch.cat(shares).numpy()
+    want = oracle.head_importance(W.bf16_bits(w.q), W.bf16_bits(w.k_cache), w.seqlens, heads, w.scale)[0, :L]
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+CASES = {"bench_replica_timing": _bench_replica_timing, "context_parallel_merge": _context_parallel_merge,
+         "context_parallel_importance": _context_parallel_importance}
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
