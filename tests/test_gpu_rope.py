@@ -181,3 +181,53 @@ def test_rope_tree_then_commit_is_a_plain_sequence():
             src = kh[b, L[b] + path[b, j]]
             want = oracle.rope_rotate(src, L[b] + j, 10000.0)  # the plain sequence position of slot L + j
             _close(gk[b, L[b] + j], want, src, torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 40), (torch.float32, 40), (torch.bfloat16, 256),
+                                     (torch.bfloat16, 2)])
+def test_rope_other_head_dims(dtype, D):
+    """D not a multiple of 16 (the one-pair-per-thread path), the largest D
+    (128 pairs) and the smallest."""
+    rng = np.random.default_rng(D)
+    B, T, Hq, Hkv = 3, 7, 4, 2
+    L = np.array([0, 17, 90], np.int32)
+    cap = int(L.max()) + T + 1
+    pos = (L[:, None] + np.arange(T) + 70000).astype(np.int32)
+    q = torch.from_numpy(rng.standard_normal((B, T, Hq, D)).astype(np.float32)).to(dtype)
+    k = torch.from_numpy(rng.standard_normal((B, cap, Hkv, D)).astype(np.float32)).to(dtype)
+    qh, kh = _host(q), _host(k)
+    want_q, want_k = oracle.rope_draft_dense(qh, kh, L, pos, 10000.0)
+    qd, kd = q.cuda(), k.cuda()
+    va.verify_rope_draft_dense(qd, kd, dev_i32(L), dev_i32(pos), 10000.0)
+    torch.cuda.synchronize()
+    _close(_host(qd), want_q, qh, dtype)
+    gk = _host(kd)
+    for b in range(B):
+        rows = slice(int(L[b]), int(L[b]) + T)
+        _close(gk[b, rows], want_k[b, rows], kh[b, rows], dtype)
+        keep = np.ones(cap, bool)
+        keep[rows] = False
+        assert np.array_equal(gk[b, keep], kh[b, keep])
+
+
+def test_rope_rows_not_16_byte_aligned():
+    """q and the cache one element past a 16-byte boundary: the vector path is
+    not taken; same results."""
+    rng = np.random.default_rng(3)
+    B, T, Hq, Hkv, D = 2, 5, 4, 2, 64
+    L = np.array([3, 40], np.int32)
+    cap = 50
+    pos = (L[:, None] + np.arange(T)).astype(np.int32)
+    qf = torch.from_numpy(rng.standard_normal(B * T * Hq * D + 1).astype(np.float32)).to(torch.bfloat16).cuda()
+    kf = torch.from_numpy(rng.standard_normal(B * cap * Hkv * D + 1).astype(np.float32)).to(torch.bfloat16).cuda()
+    qd = qf[1:].view(B, T, Hq, D)
+    kd = kf[1:].view(B, cap, Hkv, D)
+    qh, kh = _host(qd), _host(kd)
+    want_q, want_k = oracle.rope_draft_dense(qh, kh, L, pos, 10000.0)
+    va.verify_rope_draft_dense(qd, kd, dev_i32(L), dev_i32(pos), 10000.0)
+    torch.cuda.synchronize()
+    _close(_host(qd), want_q, qh, torch.bfloat16)
+    gk = _host(kd)
+    for b in range(B):
+        rows = slice(int(L[b]), int(L[b]) + T)
+        _close(gk[b, rows], want_k[b, rows], kh[b, rows], torch.bfloat16)

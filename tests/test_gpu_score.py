@@ -68,7 +68,7 @@ def _check(got, want, L, R):
 @pytest.mark.parametrize("T,heads", [(1, [1]), (5, [1, 6]), (5, [0, 1, 2]), (5, [5, 5]), (16, [3, 4]),
                                      (8, [7, 0, 3, 4, 2])])
 def test_importance_matches_oracle(T, heads):
-    """Ragged prefixes around the 256-key chunk and 1024-key block edges, one
+    """Ragged prefixes around the 128-key chunk and 1024-key block edges, one
     empty sequence; units split by kv-head and at 8 rows."""
     L = [1, 255, 256, 257, 1023, 1500, 3000, 0]
     q, k, L = _case(T * 31 + len(heads), len(L), T, 8, 2, L)
@@ -136,3 +136,14 @@ def test_importance_feeds_the_index_builder():
             rest_out = np.array(sorted(set(cand.tolist()) - set(sel.tolist())))
             if len(rest_sel) and len(rest_out):
                 assert imp_h[b, h, rest_sel].min() >= imp_h[b, h, rest_out].max()
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,heads", [(64, 8, 2, [0, 1, 4, 5]), (8, 32, 8, list(range(32)))])
+def test_importance_largest_row_counts(T, Hq, Hkv, heads):
+    """256 rows: 64 tokens of four heads on two kv-heads, and all 32 heads of
+    eight kv-heads -- the row and head limits, 32 units."""
+    L = [300, 129, 1]
+    q, k, L = _case(T + Hq, len(L), T, Hq, Hkv, L)
+    got = _run(q, k, L, heads, 0.0884)
+    want = oracle.head_importance(_bits(q), _bits(k), L, heads, 0.0884)
+    _check(got, want, L, len(heads) * T)
