@@ -297,7 +297,7 @@ def measure_rope(va, peak, steps=1024):
                         "tree positions",
             "us_per_call": round(t * 1e6, 3), "algorithmic_bytes": nbytes,
             "GBps": round(nbytes / t / 1e9, 1), "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
-            "launches_per_call": 1,
+            "launches_per_call": 1, "cpu_baseline": oracle_rate(*rope_oracle_sample()),
             "note": "about 21 MB a call: launch- and latency-bound, the rows mostly served from L2 in the loop"}
 
 
@@ -345,7 +345,7 @@ def measure_scoring(va, peak, steps=256):
                         f"16K-32K, heads {heads}",
             "us_per_call": round(t * 1e6, 3), "algorithmic_bytes": nbytes,
             "GBps": round(nbytes / t / 1e9, 1), "frac_of_measured_hbm": round(nbytes / t / 1e9 / peak, 4),
-            "launches_per_call": 2}
+            "launches_per_call": 2, "cpu_baseline": oracle_rate(*scoring_oracle_sample(w))}
 
 
 def e2e_measure(w, va, steps):
@@ -452,6 +452,47 @@ def cpu_baseline(w, target_s=12.0, max_reps=50):
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+
+def oracle_rate(fn, nbytes, sample, target_s=4.0, max_reps=20):
+    """Host-side GB/s of one oracle call ``fn`` that covers ``nbytes`` of the
+    step's algorithmic bytes, repeated until about ``target_s`` seconds."""
+    t0 = time.perf_counter()
+    reps = 0
+    while reps == 0 or (time.perf_counter() - t0 < target_s and reps < max_reps):
+        fn()
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes * reps / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{sample}; {reps} runs",
+            "seconds": round(dt, 2)}
+
+
+def scoring_oracle_sample(w, n_seq=2):
+    """The importance pass of the oracle on the first ``n_seq`` sequences of
+    workload ``w``: (callable, algorithmic bytes it covers, description)."""
+    import oracle
+
+    heads = list(w.score_heads)
+    n_kv = len({h // w.group for h in heads})
+    qb, kb = W.bf16_bits(w.q[:n_seq]), W.bf16_bits(w.k_cache[:n_seq])
+    L = w.seqlens[:n_seq]
+    nbytes = int(L.astype(np.int64).sum()) * (n_kv * w.D * 2 + w.Hkv * 4) + n_seq * w.T * len(heads) * w.D * 2
+    return (lambda: oracle.head_importance(qb, kb, L, heads, w.scale)), nbytes, \
+        f"sequences 0..{n_seq - 1} of the workload (numpy fp64, BLAS threads up to the cores)"
+
+
+def rope_oracle_sample(B=4):
+    """The oracle's rotation of the draft block on a B-sequence cut of the paged
+    workload (its own page pool): (callable, algorithmic bytes, description)."""
+    import oracle
+
+    w = W.make_workload("paged", seed=0, B=B, tree="random")
+    pos = (w.seqlens[:, None] + np.stack([W.chain_depths(p) for p in w.parent])).astype(np.int32)
+    qb, kb = W.bf16_bits(w.q), W.bf16_bits(w.k_pages)
+    nbytes = 2 * w.B * w.T * (w.Hq + w.Hkv) * w.D * 2
+    return (lambda: oracle.rope_draft_paged(qb, kb, w.page_table, w.page_size, w.seqlens, pos, 500000.0)), \
+        nbytes, f"{B} sequences of the paged workload (numpy fp64, one thread)"
 
 
 # DRAM traffic per launch of the dominant kernel, from the committed ncu capture
