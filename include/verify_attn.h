@@ -19,7 +19,11 @@
  *   after the call returns.  Only `shape` and the scalar arguments live on the
  *   host.  `workspace` is caller-owned device scratch of at least
  *   verify_attn_workspace_size() bytes, 256-byte aligned, initialised once with
- *   verify_attn_workspace_init() and reusable by later calls on the same stream.
+ *   verify_attn_workspace_init() and reusable by later calls on the same stream,
+ *   of this shape or of any other shape it is large enough for (its bookkeeping
+ *   sits at fixed offsets and every completed call returns it to zero).  After
+ *   a call that stopped at a bounded wait (verify_attn_check_status returns
+ *   VA_ERR_TIMEOUT) run verify_attn_workspace_init() again before reusing it.
  *   Calls that run concurrently (different streams) need separate workspaces.
  * Streams.  Every call only enqueues work on `stream` (NULL = legacy default
  *   stream) and returns; nothing synchronises except verify_attn_check_status.
@@ -134,7 +138,9 @@ va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_
  * about 350 (sequence, kv-head) pairs fit -- e.g. one sequence with 8 draft
  * tokens, or 16 sequences of 5; a batch of 64 sequences of 16 does not.
  * Sharing.  Every call uses the same array and leaves its contents behind;
- * each call clears the status word it needs.  Calls whose work overlaps on the
+ * each call first clears the array's bookkeeping (status word and merge
+ * counters, 16.6 KB), so a call is unaffected by the shape or the outcome of
+ * the one before it.  Calls whose work overlaps on the
  * GPU (different streams, or different host threads) race on the array and
  * give undefined results: serialise them.
  * device_status (may be NULL): a caller-owned device int32 that receives this
@@ -340,7 +346,9 @@ va_status verify_commit_kv_paged(const va_shape *shape, void *k_pages, void *v_p
                                  int32_t *seqlens_out, void *workspace, va_stream stream);
 
 /* Wait for `stream`, read and clear the device status word of `workspace`.
- * Returns VA_OK or the first device-side error recorded since the last check. */
+ * Returns VA_OK or the first device-side error recorded since the last check.
+ * After VA_ERR_TIMEOUT the workspace needs verify_attn_workspace_init() before
+ * its next attention call (a merge counter may have been left mid-count). */
 va_status verify_attn_check_status(void *workspace, va_stream stream);
 
 /* Message for the last error returned on the calling thread ("" if none). */

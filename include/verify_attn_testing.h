@@ -22,6 +22,19 @@ extern "C" {
  */
 va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long wait_ns, va_stream stream);
 
+/*
+ * Fault injection on the host side of the attention calls, for the recovery
+ * tests.  Until called again, every later attention launch of the process
+ * (a) uses wait_ns (0 < wait_ns <= 1e8) as the limit of each bounded device
+ * wait instead of the default (wait_ns = 0 restores the default), and (b) if
+ * drop_part >= 0, lets CTA number drop_part of the keys-on-lanes kernel skip
+ * announcing the segment parts it computed, as if that message were lost:
+ * the other parts of those segments then wait for it until the limit runs
+ * out, record VA_ERR_TIMEOUT and finish without merging (drop_part < 0: off).
+ * Nothing on the GPU faults or hangs; the call's outputs are undefined.
+ */
+va_status verify_attn_test_inject(unsigned long long wait_ns, int drop_part);
+
 #ifdef __cplusplus
 }
 #endif

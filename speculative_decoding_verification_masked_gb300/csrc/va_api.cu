@@ -9,6 +9,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -43,7 +44,7 @@ va_status cuda_fail(cudaError_t e, const char *what) {
   return fail(VA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-constexpr int kMaxSegments = 2048;
+using va::kMaxSegments;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per bounded wait
 
 uint64_t wait_limit_ns() {
@@ -57,6 +58,11 @@ uint64_t wait_limit_ns() {
   }();
   return v;
 }
+
+// Test hook (verify_attn_testing.h): a wait limit and a dropped part for the
+// next attention calls of the process.
+std::atomic<unsigned long long> g_test_wait_ns{0};
+std::atomic<int> g_test_drop_part{-1};
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -260,6 +266,8 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
   p.o_part = reinterpret_cast<float *>(ws + wl.o_off);
   p.wait_ns = wait_limit_ns();
+  p.test_drop_part = g_test_drop_part.load();
+  if (const unsigned long long tw = g_test_wait_ns.load()) p.wait_ns = tw;
 
   // key tiles an upper bound can produce; the grid never exceeds them
   long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
@@ -678,7 +686,10 @@ va_status verify_attn_check_status(void *workspace, va_stream stream) {
   e = cudaMemcpy(&status, workspace, sizeof status, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (status != 0) {
-    // the merge bookkeeping of a call that stopped early is reset with the status
+    // the status word and the merge kernel's list length are reset here; the
+    // per-segment merge counters of a call that stopped at a timeout may not be
+    // (their size depends on the workspace, which this call is not given):
+    // verify_attn_workspace_init restores them
     e = cudaMemset(workspace, 0, va::kHeaderBytes);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
     switch (status) {
@@ -697,7 +708,14 @@ const char *verify_attn_last_error(void) { return g_last_error.c_str(); }
 
 const char *verify_attn_version(void) { return "verify_attn 0.1 sm_103a"; }
 
-// Test hook declared in verify_attn_testing.h.
+// Test hooks declared in verify_attn_testing.h.
+va_status verify_attn_test_inject(unsigned long long wait_ns, int drop_part) {
+  if (wait_ns > 100000000ull) return fail(VA_ERR_INVALID_ARG, "wait_ns must be at most 0.1 s");
+  g_test_wait_ns.store(wait_ns);
+  g_test_drop_part.store(drop_part < 0 ? -1 : drop_part);
+  return ok();
+}
+
 va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long wait_ns, va_stream stream) {
   if (workspace == nullptr || !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "bad workspace");
   if (wait_ns == 0 || wait_ns > 100000000ull) return fail(VA_ERR_INVALID_ARG, "wait_ns must be in (0, 0.1 s]");
@@ -763,9 +781,11 @@ extern "C" va_status verify_attn_dense_noalloc(const va_shape *shape, const void
   void *scratch = nullptr;
   st = static_scratch_address(&scratch);
   if (st != VA_OK) return st;
-  // the status word must start at zero for this call's device-side checks
-  cudaError_t e = cudaMemsetAsync(scratch, 0, va::kHeaderBytes, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch status word");
+  // the bookkeeping (status word, merge list length, per-segment merge
+  // counters) starts at zero for every call, whatever the previous call's shape
+  // or outcome; the rest of the scratch is written before it is read
+  cudaError_t e = cudaMemsetAsync(scratch, 0, va::kBookkeepingBytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch bookkeeping");
   st = verify_attn_dense(shape, q, k_cache, v_cache, max_cache_len, seqlens, tree_parent, tree_mask, positions, out,
                          lse, scratch, kStaticScratchBytes, stream);
   if (st != VA_OK) return st;

@@ -265,11 +265,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
             o[i][2] *= alpha[1];
             o[i][3] *= alpha[1];
           }
-          // O += P V.  On tiles holding draft keys (where only a few keys may be
-          // visible and |out| ~ |v|), P is split into bf16 hi + lo parts so ~16
-          // bits of P survive; one bf16 P alone adds up to 2^-9 |v| of error.  On
-          // pure prefix tiles the rounding errors of many keys average out.
-          const bool exact_p = lt * kTK + kTK > g.n_prefix;
+          // O += P V with P split into bf16 hi + lo parts, so ~16 bits of every
+          // weight survive: one bf16 P alone keeps a weight only to 2^-8 of
+          // itself, which shows in the output when a few keys carry a row's
+          // weight (attention sinks, or a draft tile where few keys are visible).
+          constexpr bool exact_p = true;
 #pragma unroll
           for (int kk = 0; kk < NK / 16; ++kk) {
             uint32_t a[4], al[4];

@@ -9,10 +9,18 @@
 // Roles (11 warps when the segment has two 128-row M-tiles):
 //   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
 //                    = one TMEM lane.  Reads S from TMEM, applies the draft
-//                    bitmask, runs the online softmax, writes P (bf16; on
-//                    draft tiles also the bf16 residual) back over S, rescales
-//                    O in TMEM when the row max grows by more than 2^8, and
-//                    writes the output row.
+//                    bitmask, runs the online softmax, writes P (bf16) back
+//                    over S, rescales O in TMEM when the row max grows by more
+//                    than 2^8, and writes the output row.
+//                    A bf16 P keeps each weight only to 2^-8 of itself, which
+//                    shows in the output when a few keys carry the weight of a
+//                    row (attention sinks).  So the warpgroup votes per tile:
+//                    if the largest weight of the tile may be more than 1/16
+//                    of some row's weight so far, P's bf16 residual is written
+//                    too and its PV issuer multiplies it as well (draft tiles
+//                    always).  A key left to the bf16 P then carries at most
+//                    1/16 of its row's final weight, and on spread-out rows
+//                    only a part's first tiles take the extra MMAs.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
 //                    sparse) into a 3-stage ring (shared with the other kernel)
 //   warps 4*NMT+1+i  PV issuer of M-tile i: O_i += P_i V (A = P from TMEM, B =
@@ -52,7 +60,8 @@ struct TcSmem {
   // barriers: full[NS], empty[NS], s_full[2][2], p_full[2][2], o_done[2][2], drain
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kTstartOff = kMiscOff + 16;
+  static constexpr int kLoFlagOff = kMiscOff + 16;          // int [2][2]: P residual written, per M-tile and buffer
+  static constexpr int kTstartOff = kLoFlagOff + 16;
   static constexpr int kThreads = (5 * NMT + 2) * 32;
 };
 
@@ -74,7 +83,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   constexpr int kMmaWarp0 = 4 * NMT + 1;  // PV issuer of M-tile i is warp kMmaWarp0 + i
   constexpr int kSWarp = 5 * NMT + 1;     // S issuer of every M-tile
   constexpr int kMmaThreads = 32 * (NMT + 1);
-  constexpr int kBarQ = 1, kBarSoft = 2, kBarEnd = 3;
+  constexpr int kBarQ = 1, kBarSoft = 2, kBarEnd = 3, kBarVote = 4;  // kBarVote + M-tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *sQ = smem;
@@ -89,6 +98,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
   int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  volatile int *lo_flag = reinterpret_cast<volatile int *>(smem + SM::kLoFlagOff);
   constexpr bool use_tma = kTma;  // tiles by TMA boxes (dense, paged), else cp.async gathers
 
   const int tid = threadIdx.x;
@@ -223,8 +233,10 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
             issue_s(i, b, st);
           }
         } else {
-          const bool exact = lt * kTK + kTK > g.n_prefix;  // tile holds draft keys
           wait_ok(p_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
+          // the softmax wrote the P residual of this tile too (set before its
+          // arrive on p_full; rewritten only after this PV has completed)
+          const bool exact = lo_flag[2 * mi + b] != 0;
           acquire_stage(st, (uint32_t)(it / NS) & 1u, lt, g);
           issue_pv(mi, b, st, lt == lt0, exact);
         }
@@ -357,10 +369,15 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         }
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used * cl2;
+      // P's residual is needed where the tile's largest weight may exceed 1/16
+      // of the row's weight up to and including it: 2^(mx - mu) > (l + 2^(mx - mu)) / 16
+      bool lo = masked;
+      if (!masked) lo = bar_red_or(kBarVote + mi, 128, ex2_approx(fmaf(mx, cl2, -mu)) * 15.f > l);
+      if (r == 0) lo_flag[2 * mi + b] = lo ? 1 : 0;
       uint32_t ph[32];
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short add chains
-      if (masked) {
-        // draft tiles: P as bf16 hi + lo parts (a second MMA adds the lo parts)
+      if (lo) {
+        // P as bf16 hi + lo parts (a second set of MMAs adds the lo parts)
         uint32_t pl[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {

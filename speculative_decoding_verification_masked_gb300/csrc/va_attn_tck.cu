@@ -5,14 +5,19 @@
 // transposed, with a 128-key tile as the M side:
 //
 //   S^T (128 keys x NR rows)   = K (128 x d) . Q^T       A = K tile, K-major; B = Q, K-major
-//   O^T (128 d x NR rows)     += V^T . P^T               A = V tile, MN-major; B = P^T, MN-major
-//   l   (NR rows, every lane) += 1 (128 x 128) . P^T     A = ones held in TMEM
+//   O^T (128 d x 2NR)         += V^T . [P_hi | P_lo]^T   A = V tile, MN-major; B = P^T, MN-major
+//   l   (2NR, every lane)     += 1 (128 x 128) . [P_hi | P_lo]^T   (64 rows only; A = ones in TMEM)
 //
 // (LongSpec 2.C: the unmasked prefix and the masked draft block are the same
 // tile loop, the draft block being the last tiles of a segment; partial
 // results of a segment split over CTAs are merged by the exact log-sum-exp
-// combine.)  The row sums l come from the tensor core too, so the normaliser
-// uses exactly the bf16 P that the numerator used.
+// combine.)  P is split into a bf16 high part and the bf16 rounding of its
+// residual, and both are multiplied by ONE MMA whose N covers the two halves:
+// the accumulator columns of O_hi and O_lo sit side by side and are added in
+// the epilogue.  ~16 bits of every weight survive, so a row whose weight rests
+// on a few keys (attention sinks) keeps the exact result to well below the
+// bf16 output rounding, at no extra MMA: an MMA of N <= 128 costs the same
+// issue time as one of half that width.
 //
 // Roles (6 warps, one CTA per SM):
 //   warps 0-3  softmax: thread k owns key k of the tile (TMEM lane k) and all
@@ -22,16 +27,16 @@
 //              exponentials stay below 2^8 and O, l are rescaled when it
 //              moves); whether it must move is one block-wide vote (bar.red),
 //              and only then are the row maxima reduced across the 128 keys.
-//              P (bf16; on draft tiles also the bf16 residual) is written as
-//              the MN-major P^T operand over the K tile of the same stage,
-//              which the S MMA has finished reading.  In the epilogue thread
-//              d owns output column d.
+//              P (bf16 hi and lo parts) is written as the MN-major P^T
+//              operand over the K tile of the same stage, which the S MMA has
+//              finished reading.  In the epilogue thread d owns output column d.
 //   warp 4     producer: TMA boxes (dense) or cp.async gathers (paged, sparse)
 //              into a 3-stage ring of 128-key K and V tiles (64 KB a stage)
 //   warp 5     MMA issuer and TMEM owner: S of tile i+2 is issued as soon as
 //              the softmax of tile i has released its S buffer.
-// TMEM columns (NC = max(NR, 32)): O^T at 0, l at NC, S buffers at 2NC and
-// 3NC, the ones operand at 4NC.  Every wait is bounded; on timeout the CTA
+// TMEM columns (NC = max(NR, 32)): O^T hi at 0 and lo at NR, S buffers at 2NC
+// and 3NC, the ones operand at 4NC, l hi / lo (64 rows) at 5NC and 5NC + NR.
+// Every wait is bounded; on timeout the CTA
 // records VA_ERR_TIMEOUT, keeps the barrier sequence of all roles, drains and
 // frees TMEM.
 #include <cuda.h>
@@ -77,6 +82,10 @@ struct TkSmem {
   static_assert(kRowInvOff % 16 == 0, "vector loads of the row constants");
   static constexpr int kNC = NR < 32 ? 32 : NR;            // TMEM columns per region
   static constexpr int kTmemCols = NR <= 32 ? 256 : 512;
+  // O_hi | O_lo take columns [0, 2NR): within O and the (unused) l region for
+  // NR <= 32; for 64 rows l moves past the ones operand
+  static constexpr int kLCol = NR <= 32 ? kNC : 5 * kNC;
+  static_assert(2 * NR <= 2 * kNC && kLCol + 2 * NR <= kTmemCols, "TMEM plan");
 };
 
 // Row-wise block of a warp: v[N] per lane -> lane holds the warp maximum of
@@ -127,21 +136,6 @@ struct WarpScatterSum {
   }
 };
 
-// Block-wide OR of a predicate over the `n` threads of named barrier `id`
-// (also a barrier for them).
-__device__ __forceinline__ bool bar_red_or(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 // NR fp32 columns of this thread's TMEM lane.
 template <int NR>
 __device__ __forceinline__ void tmem_ld_f(uint32_t taddr, float (&x)[NR]) {
@@ -167,6 +161,16 @@ __device__ __forceinline__ void tmem_ld_f(uint32_t taddr, float (&x)[NR]) {
       for (int j = 0; j < 32; ++j) x[32 * h + j] = __uint_as_float(u[j]);
     }
   }
+}
+
+// O_hi + O_lo: N fp32 columns at taddr plus the N columns `lo` further on.
+template <int N>
+__device__ __forceinline__ void tmem_ld_hilo(uint32_t taddr, uint32_t lo, float (&x)[N]) {
+  float y[N];
+  tmem_ld_f<N>(taddr, x);
+  tmem_ld_f<N>(taddr + lo, y);
+#pragma unroll
+  for (int j = 0; j < N; ++j) x[j] += y[j];
 }
 
 // Multiply column j of this lane's NR columns at taddr by a[j].
@@ -381,9 +385,9 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
   if (warp == kMmaWarp) {
     // ================================ MMA issuer ================================
     const uint32_t id_s = umma_idesc(128, NR, 0, 0);
-    const uint32_t id_o = umma_idesc(128, NR, 1, 1);
-    const uint32_t id_l = umma_idesc(128, NR, 0, 1);
-    const uint32_t tO = tmem, tL = tmem + NC, tOnes = tmem + 4 * NC;
+    const uint32_t id_o = umma_idesc(128, 2 * NR, 1, 1);  // N = [P_hi | P_lo]
+    const uint32_t id_l = umma_idesc(128, 2 * NR, 0, 1);
+    const uint32_t tO = tmem, tL = tmem + SM::kLCol, tOnes = tmem + 4 * NC;
     int it = 0, jt = 0;
     // Shared-memory descriptors are built once; a K-step or stage offset is an
     // add to the start-address field (addresses stay below 256 KB, so the
@@ -391,7 +395,10 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     const uint64_t dK0 = umma_sdesc(smem_u32(stages), 16, 1024);                      // K tile, K-major
     const uint64_t dQ0 = umma_sdesc(smem_u32(sQ), 16, 1024);                          // Q, K-major
     const uint64_t dV0 = umma_sdesc(smem_u32(stages) + Geo::kTileBytes, TK * 128, 1024);  // V tile, MN-major
-    const uint64_t dP0 = umma_sdesc(smem_u32(stages), 8192, 1024);                    // P^T over the K tile
+    // P^T over the K tile: per key a 128-byte row of the hi then lo parts (N =
+    // 2NR <= 64, one swizzle atom wide), or for 64 rows hi and lo as two atoms
+    // 16 KB apart
+    const uint64_t dP0 = umma_sdesc(smem_u32(stages), TK * 128, 1024);
     constexpr uint64_t kStageStep = SM::kStageBytes >> 4;
     auto issue_s = [&](int b, int st) {  // S^T(b) = K Q^T
       if (!ok || lane != 0) return;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       }
       umma_commit(s_full + b);
     };
-    auto issue_pv = [&](int st, int b, bool first, bool exact) {  // O^T += V^T P^T, l += 1 P^T
+    auto issue_pv = [&](int st, int b, bool first) {  // [O_hi|O_lo]^T += V^T [P_hi|P_lo]^T
       if (!ok || lane != 0) return;
       tc_fence_after();
       const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
@@ -418,15 +425,6 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         const uint32_t acc = kk > 0 ? 1u : acc0;
         umma_ss(tO, dV + off, dP + off, id_o, acc);
         if constexpr (!kRegL) umma_ts(tL, tOnes, dP + off, id_l, acc);
-      }
-      if (exact) {  // the bf16 residual of P on draft tiles
-        constexpr uint64_t lo = (uint64_t)((TK * 128) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < TK / 16; ++kk) {
-          const uint64_t off = (uint64_t)((kk * 2048) >> 4);
-          umma_ss(tO, dV + off, dP + lo + off, id_o, 1u);
-          if constexpr (!kRegL) umma_ts(tL, tOnes, dP + lo + off, id_l, 1u);
-        }
       }
       umma_commit(o_done + b);
       umma_commit(empty + st);  // the stage is free once these MMAs have read it
@@ -445,9 +443,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       }
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int b = jt & 1;
-        const bool exact = lt * TK + TK > g.n_prefix;  // tile holds draft keys
         wait_ok(p_full + b, (uint32_t)(jt >> 1) & 1u);
-        issue_pv(it % NS, b, lt == lt0, exact);
+        issue_pv(it % NS, b, lt == lt0);
         if (lt + 2 < lt1) {
           wait_ok(full + (it + 2) % NS, (uint32_t)((it + 2) / NS) & 1u);
           issue_s(b, (it + 2) % NS);
@@ -468,7 +465,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 
   // ================================== softmax ==================================
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tO = tmem + lane_base, tL = tO + NC;
+  const uint32_t tO = tmem + lane_base, tL = tO + SM::kLCol;
   {  // the all-ones A operand of the row-sum MMA: 8 columns of bf16 pairs (1.0, 1.0)
     uint32_t ones[8];
 #pragma unroll
@@ -515,7 +512,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     float mu[NR];  // reference max per row, log2 units
 #pragma unroll
     for (int r = 0; r < NR; ++r) mu[r] = -INFINITY;
-    // (kRegL) sums over this thread's keys of the bf16 P the PV MMAs multiply
+    // (kRegL) sums over this thread's keys of P (the fp32 weights, which the
+    // bf16 hi + lo parts the PV MMA multiplies carry to ~2^-16)
     float lsum[kRegL ? NR : 1];
 #pragma unroll
     for (int r = 0; r < (kRegL ? NR : 1); ++r) lsum[r] = 0.f;
@@ -613,14 +611,27 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
           wait_ok(o_done + (b ^ 1), (uint32_t)((jt - 1) >> 1) & 1u);  // O and l hold every PV up to tile jt-1
           tc_fence_after();
           tmem_scale_cols<NR>(tO, x);
-          if constexpr (!kRegL) tmem_scale_cols<NR>(tL, x);
+          tmem_scale_cols<NR>(tO + NR, x);
+          if constexpr (!kRegL) {
+            tmem_scale_cols<NR>(tL, x);
+            tmem_scale_cols<NR>(tL + NR, x);
+          }
           tmem_st_wait();
         }
         load_scores();
       }
-      // P^T row of this key over the K tile of the stage (the S MMA is done with it)
+      // P^T row of this key over the K tile of the stage (the S MMA is done with
+      // it): chunk cc of the hi part, and of the lo part NR/8 chunks further
+      // (64 rows: in the second swizzle atom, 16 KB further)
       uint8_t *pk = stages + st * SM::kStageBytes;
       const int sw = tid & 7;
+      auto put_p = [&](int cc, const uint32_t (&h)[4], const uint32_t (&l)[4]) {
+        *reinterpret_cast<uint4 *>(pk + tid * 128 + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        if constexpr (NR <= 32)
+          *reinterpret_cast<uint4 *>(pk + tid * 128 + (((cc + NR / 8) ^ sw) << 4)) = make_uint4(l[0], l[1], l[2], l[3]);
+        else
+          *reinterpret_cast<uint4 *>(pk + TK * 128 + tid * 128 + ((cc ^ sw) << 4)) = make_uint4(l[0], l[1], l[2], l[3]);
+      };
       if (masked) {
 #pragma unroll
         for (int cc = 0; cc < NR / 8; ++cc) {
@@ -632,14 +643,12 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
             const float a = ex2_approx(fmaf(x[r], cl2, mu[r] == -INFINITY ? 0.f : -mu[r]));
             const float bq = ex2_approx(fmaf(x[r + 1], cl2, mu[r + 1] == -INFINITY ? 0.f : -mu[r + 1]));
             split_bf16x2(a, bq, h[q], l[q]);
-            if constexpr (kRegL) {  // exactly the bf16 hi + lo the MMAs multiply
-              lsum[r] += __uint_as_float(h[q] << 16) + __uint_as_float(l[q] << 16);
-              lsum[r + 1] += __uint_as_float(h[q] & 0xFFFF0000u) + __uint_as_float(l[q] & 0xFFFF0000u);
+            if constexpr (kRegL) {
+              lsum[r] += a;
+              lsum[r + 1] += bq;
             }
           }
-          const int off = tid * 128 + ((cc ^ sw) << 4);
-          *reinterpret_cast<uint4 *>(pk + off) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4 *>(pk + TK * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+          put_p(cc, h, l);
         }
         if (use_tma && key >= g.nkeys) {
           // rows past the segment end: TMA brought whatever follows; zero V so 0 * V stays 0
@@ -652,17 +661,19 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         // every row sees every key of a prefix tile, so mu is finite here
 #pragma unroll
         for (int cc = 0; cc < NR / 8; ++cc) {
-          uint32_t h[4];
+          uint32_t h[4], l[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = 8 * cc + 2 * q;
-            h[q] = pack_bf16(ex2_approx(fmaf(x[r], cl2, -mu[r])), ex2_approx(fmaf(x[r + 1], cl2, -mu[r + 1])));
+            const float a = ex2_approx(fmaf(x[r], cl2, -mu[r]));
+            const float bq = ex2_approx(fmaf(x[r + 1], cl2, -mu[r + 1]));
+            split_bf16x2(a, bq, h[q], l[q]);
             if constexpr (kRegL) {
-              lsum[r] += __uint_as_float(h[q] << 16);
-              lsum[r + 1] += __uint_as_float(h[q] & 0xFFFF0000u);
+              lsum[r] += a;
+              lsum[r + 1] += bq;
             }
           }
-          *reinterpret_cast<uint4 *>(pk + tid * 128 + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          put_p(cc, h, l);
         }
       }
       fence_proxy_async_smem();
@@ -696,7 +707,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < NR / CH; ++h) {
         float lv[CH];
-        tmem_ld_f<CH>(tL + h * CH, lv);
+        tmem_ld_hilo<CH>(tL + h * CH, NR, lv);
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
           my_l = tid == h * CH + j ? lv[j] : my_l;
@@ -729,7 +740,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float ov[HR];
-          tmem_ld_f<HR>(tO + half * HR, ov);
+          tmem_ld_hilo<HR>(tO + half * HR, NR, ov);
           if (ok) {
 #pragma unroll
             for (int j = 0; j < HR; j += 4) {
@@ -745,7 +756,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         // return to zero): the block barrier orders every thread's row and lse
         // stores before thread 0's release increment, which is cumulative
         named_bar_sync(kBarSoft, kSoft);
-        if (tid == 0) red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+        if (tid == 0 && c != p.test_drop_part)
+          red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
       } else {
         // 64 rows (registers are short): rows staged row-major in the Q buffer,
         // two halves of NR/2 rows written by bulk copies
@@ -753,7 +765,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float ov[HR];
-          tmem_ld_f<HR>(tO + half * HR, ov);
+          tmem_ld_hilo<HR>(tO + half * HR, NR, ov);
 #pragma unroll
           for (int j = 0; j < HR; j += 4) {
             const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + half * HR + j);
@@ -776,7 +788,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         named_bar_sync(kBarSoft, kSoft);
         if (tid == 0) {
           bulk_wait_all();
-          red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+          if (c != p.test_drop_part)
+            red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
         }
       }
       if (n_split < 2) {
@@ -792,7 +805,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < NR / CH; ++h) {
         float ov[CH];
-        tmem_ld_f<CH>(tO + h * CH, ov);
+        tmem_ld_hilo<CH>(tO + h * CH, NR, ov);
 #pragma unroll
         for (int j = 0; j < CH; j += 4) {
           const float4 inv4 = *reinterpret_cast<const float4 *>(row_inv + h * CH + j);

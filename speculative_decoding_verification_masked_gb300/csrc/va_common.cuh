@@ -16,19 +16,27 @@ namespace va {
 //   [0, 256)            header: int status word (first device-side error) at 0,
 //                       split-list length at kSplitCountOff, merge-blocks-done
 //                       count at kSplitDoneOff (both back to 0 after every merge)
+//   mcnt   int2[kMaxSegments]  per segment: the in-kernel merge counter (x;
+//                       back to 0 at the end of every call).  At a fixed offset
+//                       for every shape, so one workspace serves calls of any
+//                       shape it is large enough for.
 //   meta   int2[S]      per segment: first partial slot, number of parts
 //   split  int4[slots]  segments cut over more than one CTA (the merge's work
 //                       list): segment, first partial slot, number of parts
-//   mcnt   int2[S]      per segment: the in-kernel merge counter (x; back to 0
-//                       at the end of every call)
 //   lse_p  f32 [slots][rows_pad]
 //   o_p    f32 [slots][rows_pad][D]
+// The header and the counters are the bookkeeping that must start at zero
+// (kBookkeepingBytes); everything after it is written before it is read.
 // ---------------------------------------------------------------------------
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kSplitCountOff = 64;
 constexpr size_t kSplitDoneOff = 128;
+constexpr int kMaxSegments = 2048;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr size_t kMergeCntOff = kHeaderBytes;
+constexpr size_t kBookkeepingBytes = kMergeCntOff + ((sizeof(int2) * (size_t)kMaxSegments + 255) & ~size_t(255));
 
 struct WsLayout {
   size_t meta_off, split_off, mcnt_off, lse_off, o_off, total;
@@ -36,10 +44,10 @@ struct WsLayout {
 
 __host__ __device__ inline WsLayout ws_layout(int S, int slots, int rows_pad, int D) {
   WsLayout w;
-  w.meta_off = kHeaderBytes;
+  w.mcnt_off = kMergeCntOff;
+  w.meta_off = kBookkeepingBytes;
   w.split_off = w.meta_off + align256(sizeof(int2) * (size_t)S);
-  w.mcnt_off = w.split_off + align256(sizeof(int4) * (size_t)slots);
-  w.lse_off = w.mcnt_off + align256(sizeof(int2) * (size_t)S);
+  w.lse_off = w.split_off + align256(sizeof(int4) * (size_t)slots);
   w.o_off = w.lse_off + align256(sizeof(float) * (size_t)slots * rows_pad);
   w.total = w.o_off + align256(sizeof(float) * (size_t)slots * rows_pad * D);
   return w;
@@ -210,6 +218,21 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uin
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Block-wide OR of a predicate over the `n` threads of named barrier `id`
+// (also a barrier for them).
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 // Programmatic dependent launch controls.

@@ -49,6 +49,7 @@ struct AttnParams {
   int2 *merge_cnt;                // per segment: in-kernel merge counter (.x)
   float *lse_part, *o_part;
   uint64_t wait_ns;
+  int test_drop_part;  // test hook: this CTA's parts of split segments never arrive (-1: off)
 };
 
 size_t attn_smem_required(const AttnParams &p);

@@ -1,7 +1,6 @@
 """GPU parity at the measured workloads' full sizes, in the same launch
-configuration the benchmark times.  chain, sparse and paged are compared on
-every output; tree on two whole kv-head groups (8 of 32 heads, all 64 draft
-tokens), which the oracle computes in seconds."""
+configuration the benchmark times, on every output (the 131,072-token tree
+workload's oracle takes about 20 s on 8 host cores)."""
 import numpy as np
 import pytest
 import torch
@@ -40,18 +39,10 @@ def test_full_sparse_with_library_index():
     compare(out, lse, ref, strict=True)
 
 
-def test_full_tree_two_head_groups():
+def test_full_tree_every_head():
+    """The long-context tree workload on all 32 heads, every output."""
     w = W.make_workload("tree")
     out, lse = run_library(w, "parent")
-    out = out.float().cpu().numpy()
-    lse = lse.cpu().numpy()
-    g = w.group
-    vis = oracle.draft_visibility(w)
-    q = W.bf16_bits(w.q)
-    k = W.bf16_bits(w.k_cache)
-    v = W.bf16_bits(w.v_cache)
-    for h in (0, w.Hkv - 1):
-        ro, rl = oracle.attention_dense(q[:, :, h * g:(h + 1) * g], k[:, :, h:h + 1], v[:, :, h:h + 1], w.seqlens,
-                                        vis, w.scale)
-        assert np.abs(out[:, :, h * g:(h + 1) * g] - ro).max() <= 2e-3
-        assert np.abs(lse[:, h * g:(h + 1) * g] - rl).max() <= 1e-3
+    ref = oracle.verify(w)
+    eo, el, mx = compare(out, lse, ref, strict=True)
+    print(f"tree: max|err| out {eo:.2e} lse {el:.2e} max|out| {mx:.3f}")
