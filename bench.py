@@ -3,23 +3,29 @@
 One *step* is one verification pass over one batch of the workload: the draft
 tree's ancestor mask, the split-KV prefix pass, the masked draft-block pass and
 the log-sum-exp merge (the sparse workload adds the verify-index build).  The
-default workload is the 8-token draft chain over a 32768-token bf16 cache
-(B1, Hq32, Hkv8, d128).
+headline workload is the long-context token tree: a 64-node tree of depth 6
+over a 131072-token bf16 cache (B1, Hq32, Hkv8, d128); every other measured
+workload (chain, sparse, paged, tiny) is reported under ``other_configs`` with
+the same evidence.
 
 Reported (one JSON line on rank 0):
   value        algorithmic KV bytes of all ranks / max-over-ranks time, GB/s
                (KV bytes = (prefix keys + T) * d * 2 (K, V) * elem per kv-head)
   tokens_per_s verified draft tokens per second
-  roofline     the verification call's achieved GB/s (CUDA events per call)
-               against the measured HBM copy bandwidth
+  roofline     the dominant kernel's achieved GB/s (bytes per launch over its
+               CUDA-event duration) against the measured HBM copy bandwidth
+  sustained    the same step replayed for at least 0.6 s with the SM clocks
+               sampled every 20 ms (dozens of samples under load)
   e2e          the same metric through the public API with host buffers:
                per step, H2D of the step's new inputs (q, the draft tokens'
-               K/V rows, tree parents, seqlens), the call, D2H of out + lse
+               K/V rows, tree parents, seqlens), the call, D2H of out + lse;
+               two input sets used in turn, so the copies of the neighbouring
+               steps overlap this step's call on a second stream
   cpu_baseline the fp64 oracle timed on this host's cores (a baseline only)
 
-Timing: W warm-up steps, then K steps replayed from CUDA graphs; each step
-reads a different copy of the inputs and the copies together exceed the L2
-cache, so no step is served from L2.  Under torchrun every rank runs its own
+Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs; each
+step reads a different copy of the inputs and the copies together exceed the
+L2 cache, so no step is served from L2.  Under torchrun every rank runs its own
 replica (no collective on the data path).
 """
 from __future__ import annotations
@@ -125,7 +131,7 @@ class ClockSampler:
             self.path = f"/tmp/va_clocks_{os.getpid()}.csv"
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", phys, f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -349,9 +355,14 @@ def measure_scoring(va, peak, steps=256):
 
 
 def e2e_measure(w, va, steps):
-    """Through the public API with host buffers: per step H2D the new inputs from
-    pinned memory, run the call, D2H out and lse, and wait for them."""
-    case = DeviceCase(w, va)
+    """Through the public API with host buffers.  Every step copies its new
+    inputs from pinned host memory to the device, runs the call, and copies out
+    and lse back to pinned host memory.  Two device input sets are used in
+    turn: the uploads of step i+1 and the read-back of step i-1 run on a copy
+    stream, ordered by events around step i's call on the compute stream, so
+    only the first upload and the last read-back are not hidden; one
+    synchronisation at the end.  Returns (seconds per step, H2D bytes, D2H bytes)."""
+    cases = [DeviceCase(w, va), DeviceCase(w, va)]
     T, B = w.T, w.B
     pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
     h_q = pin(w.q)
@@ -359,63 +370,92 @@ def e2e_measure(w, va, steps):
     h_par = pin(torch.from_numpy(np.asarray(w.parent, np.int32))) if w.parent is not None else None
     h_mask = (pin(torch.from_numpy(np.ascontiguousarray(w.mask_words).view(np.int32)))
               if w.mask_words is not None else None)
-    # the draft tokens' new K/V rows, appended at slots L_b .. L_b+T-1
-    if w.layout == "paged":
-        h_knew = [pin(torch.stack([w.k_pages[w.page_table[b, (int(w.seqlens[b]) + j) // w.page_size],
-                                             (int(w.seqlens[b]) + j) % w.page_size] for j in range(T)]))
-                  for b in range(B)]
-        h_vnew = [pin(torch.stack([w.v_pages[w.page_table[b, (int(w.seqlens[b]) + j) // w.page_size],
-                                             (int(w.seqlens[b]) + j) % w.page_size] for j in range(T)]))
-                  for b in range(B)]
-    else:
-        h_knew = [pin(w.k_cache[b, int(w.seqlens[b]): int(w.seqlens[b]) + T]) for b in range(B)]
-        h_vnew = [pin(w.v_cache[b, int(w.seqlens[b]): int(w.seqlens[b]) + T]) for b in range(B)]
-    h_out = torch.empty_like(h_q).pin_memory()
-    h_lse = torch.empty(B, w.Hq, T, dtype=torch.float32).pin_memory()
+    # the draft tokens' new K/V rows, appended at slots L_b .. L_b+T-1: one copy
+    # per (sequence, page) run of slots (dense: one per sequence)
+    runs = []  # (b, first slot, n slots, page or -1)
+    for b_ in range(B):
+        L = int(w.seqlens[b_])
+        j = 0
+        while j < T:
+            if w.layout == "paged":
+                slot = L + j
+                n = min(T - j, w.page_size - slot % w.page_size)
+                runs.append((b_, slot, n, int(w.page_table[b_, slot // w.page_size])))
+            else:
+                n = T
+                runs.append((b_, L + j, n, -1))
+            j += n
+
+    def src_rows(kv, b_, slot, n, page):
+        if page >= 0:
+            pages = w.k_pages if kv == 0 else w.v_pages
+            return pin(pages[page, slot % w.page_size: slot % w.page_size + n])
+        cache = w.k_cache if kv == 0 else w.v_cache
+        return pin(cache[b_, slot: slot + n])
+
+    h_new = [(src_rows(0, *r), src_rows(1, *r)) for r in runs]
+    h_out = [torch.empty_like(h_q).pin_memory() for _ in range(2)]
+    h_lse = [torch.empty(B, w.Hq, T, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = h_q.numel() * h_q.element_size() + h_seq.numel() * 4
     h2d += (h_par.numel() * 4 if h_par is not None else 0) + (h_mask.numel() * 4 if h_mask is not None else 0)
-    h2d += sum(t.numel() * t.element_size() for t in h_knew + h_vnew)
+    h2d += sum(a.numel() * a.element_size() + c.numel() * c.element_size() for a, c in h_new)
     if w.layout == "sparse":
         h_sd = pin(torch.from_numpy(w.score_draft))
         h_st = pin(torch.from_numpy(w.score_target))
         h2d += 2 * h_sd.numel() * 4
-    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+    d2h = h_out[0].numel() * h_out[0].element_size() + h_lse[0].numel() * 4
 
-    def upload():
+    def upload(case):
         case.q.copy_(h_q, non_blocking=True)
         case.seqlens.copy_(h_seq, non_blocking=True)
         if h_par is not None:
             case.parent.copy_(h_par, non_blocking=True)
         if h_mask is not None:
             case.mask.copy_(h_mask, non_blocking=True)
-        for b in range(B):
-            L = int(w.seqlens[b])
-            if w.layout == "paged":
-                for j in range(T):
-                    pg = int(w.page_table[b, (L + j) // w.page_size])
-                    case.k[pg, (L + j) % w.page_size].copy_(h_knew[b][j], non_blocking=True)
-                    case.v[pg, (L + j) % w.page_size].copy_(h_vnew[b][j], non_blocking=True)
+        for (b_, slot, n, page), (hk, hv) in zip(runs, h_new):
+            if page >= 0:
+                r0 = slot % w.page_size
+                case.k[page, r0: r0 + n].copy_(hk, non_blocking=True)
+                case.v[page, r0: r0 + n].copy_(hv, non_blocking=True)
             else:
-                case.k[b, L: L + T].copy_(h_knew[b], non_blocking=True)
-                case.v[b, L: L + T].copy_(h_vnew[b], non_blocking=True)
+                case.k[b_, slot: slot + n].copy_(hk, non_blocking=True)
+                case.v[b_, slot: slot + n].copy_(hv, non_blocking=True)
         if w.layout == "sparse":
             case.sd.copy_(h_sd, non_blocking=True)
             case.st.copy_(h_st, non_blocking=True)
 
-    def one():
-        upload()
-        case.step()
-        h_out.copy_(case.out, non_blocking=True)
-        h_lse.copy_(case.lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    up_done = [torch.cuda.Event(), torch.cuda.Event()]
+    call_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    for _ in range(3):
-        one()
+    def run(n_steps):
+        with torch.cuda.stream(copy):
+            upload(cases[0])
+            up_done[0].record(copy)
+        for i in range(n_steps):
+            s = i & 1
+            if i + 1 < n_steps:  # next step's inputs into the other set, once its last call is done
+                with torch.cuda.stream(copy):
+                    if i >= 1:
+                        copy.wait_event(call_done[s ^ 1])
+                    upload(cases[s ^ 1])
+                    up_done[s ^ 1].record(copy)
+            comp.wait_event(up_done[s])
+            cases[s].step()
+            call_done[s].record(comp)
+            with torch.cuda.stream(copy):  # this step's result back to the host
+                copy.wait_event(call_done[s])
+                h_out[s].copy_(cases[s].out, non_blocking=True)
+                h_lse[s].copy_(cases[s].lse, non_blocking=True)
+        torch.cuda.synchronize()
+
+    run(4)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    run(steps)
     dt = (time.perf_counter() - t0) / steps
-    va.verify_attn_check_status(case.ws)
+    for c in cases:
+        va.verify_attn_check_status(c.ws)
     return dt, h2d, d2h
 
 
@@ -451,7 +491,7 @@ def cpu_baseline(w, target_s=12.0, max_reps=50):
         sample = f"{reps} full passes of the workload"
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 4)}
 
 
 def oracle_rate(fn, nbytes, sample, target_s=4.0, max_reps=20):
@@ -495,13 +535,10 @@ def rope_oracle_sample(B=4):
         nbytes, f"{B} sequences of the paged workload (numpy fp64, one thread)"
 
 
-# DRAM traffic per launch of the dominant kernel, from the committed ncu capture
-# named here (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
-# the sources that kernel is built from are byte-identical to those captured.
-PROFILED_TRAFFIC = {
-    "chain": {"sha256": "f8e4383d9fe7ee8a8d93194bbbc0cb40c44278aa19b814c26cfd24a8e38b21fa", "bytes": 134499072 + 3679744,
-              "summary": "profiles/verify_attn_tck_chain.md"},
-}
+# DRAM traffic per launch of the dominant kernel from one ncu capture of it
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the sources
+# that kernel is built from hash to those captured.
+PROFILED_TRAFFIC = {}
 KERNEL_SOURCES = ["va_attn_tck.cu", "va_pipeline.cuh", "va_common.cuh", "va_tcgen05.cuh", "va_kernels.h"]
 
 
@@ -524,7 +561,8 @@ def profiled_traffic(config):
 
 
 def attention_path(w):
-    """Which kernels one verification call launches (mirrors the library's row plan)."""
+    """The dominant kernel of one verification call and the launches of one
+    step (mirrors the library's row plan)."""
     R = (w.Hq // w.Hkv) * w.T
     small_rows = w.dtype == "bf16" and w.D == 128 and R <= 64 and os.environ.get("VA_SMALL_ROWS_KERNEL") != "mma"
     if small_rows:
@@ -533,7 +571,7 @@ def attention_path(w):
     elif w.dtype == "bf16" and w.D == 128:
         kernel, launches = "verify_attn_tc_kernel (rows on TMEM lanes) + split-segment merge kernel", 2
     else:
-        kernel, launches = "verify_attn_kernel (mma.sync) + split-segment merge kernel", 2
+        kernel, launches = "verify_attn_kernel (mma.sync / fp32 SIMT) + split-segment merge kernel", 2
     if w.layout == "sparse":
         launches += 1  # the verify-index build
     return kernel, launches
@@ -678,17 +716,23 @@ def config_dict(w, n_copies):
     return d
 
 
-def measure_config(name, va, args, want_e2e, want_cpu, rank, dist):
-    w = W.make_workload(name, seed=0)
-    n_copies = n_copies_for(w)
-    cases = [DeviceCase(w, va)] + []
-    for _ in range(n_copies - 1):
-        cases.append(DeviceCase(w, va))
-    graph_steps = min(max(args.steps, 1), 64)
-    graph, reps = time_graph_steps(cases, args.steps, args.warmup, graph_steps)
-    steps_done = reps * graph_steps
-    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    time.sleep(0.2 if clocks else 0)
+def nvtx(name):
+    """An NVTX range around a bench phase (visible in a profiler timeline)."""
+    class _R:
+        def __enter__(self):
+            torch.cuda.nvtx.range_push(name)
+
+        def __exit__(self, *a):
+            torch.cuda.nvtx.range_pop()
+    return _R()
+
+
+def replay_timed(graph, reps, rank, dist, sample_clocks):
+    """CUDA-event seconds of ``reps`` graph replays on the current stream,
+    bracketed by barrier + synchronize; optionally with the SM clocks sampled."""
+    clocks = ClockSampler(torch.cuda.current_device()) if (sample_clocks and rank == 0) else None
+    if clocks:
+        time.sleep(0.1)
     barrier(dist)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -699,41 +743,134 @@ def measure_config(name, va, args, want_e2e, want_cpu, rank, dist):
     e1.record()
     torch.cuda.synchronize()
     barrier(dist)
-    dt = e0.elapsed_time(e1) * 1e-3 / steps_done
     clk = clocks.stop() if clocks else None
+    return e0.elapsed_time(e1) * 1e-3, clk
+
+
+class AttentionOnly:
+    """The attention call of a sparse step alone (the verify sets built once
+    beforehand), to time the dominant kernel without the index build."""
+
+    def __init__(self, case):
+        self.case = case
+        case.va.verify_build_index(case.seqlens, case.sd, case.st, case.w.n_sink, case.w.window, case.w.m_draft,
+                                   case.w.budget, indices=case.idx, n_indices=case.nidx, workspace=case.ws)
+
+    def step(self):
+        c, w = self.case, self.case.w
+        c.va.verify_attn_sparse(c.q, c.k, c.v, c.seqlens, c.idx, c.nidx, tree_parent=c.parent, tree_mask=c.mask,
+                                out=c.out, lse=c.lse, workspace=c.ws, scale=w.scale)
+
+
+def measure_config(name, va, args, peak, peak_kind, want_e2e, want_cpu, rank, dist, cpu_s):
+    """Everything reported for one workload: exactly K timed steps (after W
+    warm-up steps), a sustained region of at least 0.6 s with clocks, the
+    dominant kernel's roofline, per-call percentiles, e2e and the oracle."""
+    w = W.make_workload(name, seed=0)
+    world = dist.get_world_size() if dist is not None else 1
+    n_copies = n_copies_for(w)
+    cases = [DeviceCase(w, va) for _ in range(n_copies)]
+    bytes_step = w.kv_bytes()
+    kernel, launches = attention_path(w)
+    res = {"w": w, "n_copies": n_copies, "kernel": kernel, "launches": launches}
+    with nvtx(f"{name}: warm-up"):
+        graph_steps = min(max(args.steps, 1), 64)
+        graph, _ = time_graph_steps(cases, 0, 0, graph_steps)
+        # W warm-up steps, then exactly K steps: graphs of `graph_steps` steps,
+        # and a remainder graph for K not a multiple of it
+        full, rem = divmod(args.steps, graph_steps)
+        g_rem = time_graph_steps(cases, 0, 0, rem)[0] if rem else None
+        g_w, _ = time_graph_steps(cases, 0, 0, 1)
+        for _ in range(args.warmup):
+            g_w.replay()
+        torch.cuda.synchronize()
+    with nvtx(f"{name}: timed K steps"):
+        clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(full):
+            graph.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(dist)
+        dt = e0.elapsed_time(e1) * 1e-3 / args.steps
+    with nvtx(f"{name}: sustained"):
+        reps = max(1, math.ceil(0.6 / max(dt * graph_steps, 1e-6)))
+        sus_t, _ = replay_timed(graph, reps, rank, dist, sample_clocks=False)
+        clk = clocks.stop() if clocks else None
+    sus_dt = sus_t / (reps * graph_steps)
     for c in cases:
         va.verify_attn_check_status(c.ws)
     dt_max = max_over_ranks(dt, dist)
-    world = dist.get_world_size() if dist is not None else 1
-    bytes_step = w.kv_bytes()
-    gbs = whole_job_rate(bytes_step, dt, dist) / 1e9
-    durs = per_call_durations(cases, 200)
-    call_s = statistics.mean(durs)
+    sus_max = max_over_ranks(sus_dt, dist)
+    res.update(dt=dt_max, gbs=whole_job_rate(bytes_step, dt, dist) / 1e9, tok_s=w.tokens() * world / dt_max,
+               steps=args.steps, clocks=clk,
+               sustained={"us_per_step": round(sus_max * 1e6, 3), "steps": reps * graph_steps,
+                          "seconds": round(sus_t, 3), "GBps": round(bytes_step / sus_max / 1e9, 1),
+                          "frac_of_measured_hbm": round(bytes_step / sus_max / 1e9 / peak, 4)})
+    # the dominant kernel: the step itself when it is one launch; the sparse
+    # attention timed alone; otherwise the whole call (its launches together)
+    with nvtx(f"{name}: kernel"):
+        if w.layout == "sparse":
+            kcases = [AttentionOnly(c) for c in cases]
+            kg, kreps = time_graph_steps(kcases, 64 * max(1, math.ceil(0.1 / max(sus_dt * 64, 1e-6))), 3, 64)
+            kt, _ = replay_timed(kg, kreps, rank, dist, sample_clocks=False)
+            kern_s, kern_from = kt / (kreps * 64), "attention calls alone, CUDA events over graph replays"
+            del kg
+        else:
+            kern_s = dt_max
+            kern_from = "timed region / steps" + ("" if launches == 1 else " (all launches of the call)")
+    with nvtx(f"{name}: per-call"):
+        durs = per_call_durations(cases, 200)
     call_pct = [float(x) for x in np.percentile(np.asarray(durs, dtype=np.float64), [10, 50, 90])]
-    res = {"w": w, "dt": dt_max, "gbs": gbs, "tok_s": w.tokens() * world / dt_max, "call_s": call_s,
-           "call_gbs": bytes_step / call_s / 1e9, "call_pct": call_pct, "clocks": clk, "n_copies": n_copies,
-           "steps": steps_done}
+    traffic = profiled_traffic(name)
+    res["roofline"] = {"bound": "hbm", "achieved": round(bytes_step / kern_s / 1e9, 1), "peak": peak, "unit": "GB/s",
+                       "frac": round(bytes_step / kern_s / 1e9 / peak, 4), "traffic": traffic,
+                       "kernel": kernel, "kernel_us": round(kern_s * 1e6, 3), "kernel_us_from": kern_from,
+                       "call_us": round(statistics.mean(durs) * 1e6, 3),
+                       "call_us_p10_p50_p90": [round(x * 1e6, 3) for x in call_pct], "peak_kind": peak_kind}
+    del graph, g_w, g_rem, cases
+    torch.cuda.empty_cache()
     if want_e2e:
-        e_dt, h2d, d2h = e2e_measure(w, va, max(20, min(args.steps, 200)))
+        with nvtx(f"{name}: e2e"):
+            e_dt, h2d, d2h = e2e_measure(w, va, max(50, min(args.steps * 10, 400)))
         e_dt = max_over_ranks(e_dt, dist)
         res["e2e"] = {"value": round(bytes_step * world / e_dt / 1e9, 2), "unit": "GB/s",
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": round(e_dt * 1e3, 4)}
+        torch.cuda.empty_cache()
     if want_cpu and rank == 0:
-        res["cpu"] = cpu_baseline(w)
-    del graph, cases
-    torch.cuda.empty_cache()
+        with nvtx(f"{name}: oracle on the host"):
+            res["cpu"] = cpu_baseline(w, target_s=cpu_s)
     return res
+
+
+def config_entry(r, world, peak):
+    """The other_configs entry of one measured workload."""
+    d = {"workload": config_dict(r["w"], r["n_copies"])["workload"],
+         "GBps": round(r["gbs"] / world, 1), "frac_of_measured_hbm": round(r["gbs"] / world / peak, 4),
+         "us_per_step": round(r["dt"] * 1e6, 3), "steps": r["steps"], "tokens_per_s": round(r["tok_s"] / world, 1),
+         "kv_bytes_per_step": r["w"].kv_bytes(), "gpu_launches_per_step": r["launches"],
+         "roofline": r["roofline"], "sustained": r["sustained"], "clocks": r["clocks"]}
+    if "cpu" in r:
+        d["cpu_baseline"] = r["cpu"]
+    return d
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="chain", choices=list(W.CONFIG_NAMES))
-    ap.add_argument("--all-configs", action="store_true", help="also measure every other workload")
+    ap.add_argument("--config", default="tree", choices=list(W.CONFIG_NAMES))
+    ap.add_argument("--only", action="store_true", help="measure the --config workload alone")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also the steps before and after verification (rotation, importance, acceptance, commit)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile", choices=list(W.CONFIG_NAMES) + ["after", "score", "rope"], default=None,
                     help="run --calls plain verification steps of one workload (for ncu) and exit; "
@@ -744,6 +881,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.steps < 1:
+        args.steps = 1
     if args.impl == "reference":
         return run_reference(args)
     if args.profile is not None:
@@ -755,17 +894,17 @@ def main():
     va.api.lib(build_if_missing=(rank == 0))
     barrier(dist)
     peak, peak_kind = load_peak_hbm()
-    main_res = measure_config(args.config, va, args, want_e2e=True, want_cpu=not args.no_cpu, rank=rank, dist=dist)
+    want_cpu = not args.no_cpu
+    main_res = measure_config(args.config, va, args, peak, peak_kind, want_e2e=True, want_cpu=want_cpu, rank=rank,
+                              dist=dist, cpu_s=12.0)
     others = {}
-    if args.all_configs:
+    if not args.only:
         for name in W.CONFIG_NAMES:
             if name == args.config:
                 continue
-            r = measure_config(name, va, args, want_e2e=False, want_cpu=False, rank=rank, dist=dist)
-            others[name] = {"GBps": round(r["gbs"] / world, 1), "frac_of_measured_hbm": round(r["gbs"] / world / peak, 4),
-                            "us_per_step": round(r["dt"] * 1e6, 2), "tokens_per_s": round(r["tok_s"] / world, 1),
-                            "call_us": round(r["call_s"] * 1e6, 2),
-                            "call_us_p10_p50_p90": [round(x * 1e6, 2) for x in r["call_pct"]]}
+            r = measure_config(name, va, args, peak, peak_kind, want_e2e=False, want_cpu=want_cpu, rank=rank,
+                               dist=dist, cpu_s=5.0)
+            others[name] = config_entry(r, world, peak)
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
     rope = measure_rope(va, peak) if args.all_configs and rank == 0 else None
@@ -774,13 +913,6 @@ def main():
             dist.destroy_process_group()
         return 0
     w = main_res["w"]
-    kernel_name, launches = attention_path(w)
-    # the dominant kernel's average launch duration: with one launch per step
-    # it is the timed region (CUDA events around the graph replays) divided by
-    # the steps; otherwise the mean of CUDA-event intervals around single calls
-    # (which also hold the other launches of the call)
-    kern_s = main_res["dt"] if launches == 1 else main_res["call_s"]
-    kern_gbs = w.kv_bytes() / kern_s / 1e9
     line = {
         "metric": METRIC,
         "value": round(main_res["gbs"], 2),
@@ -797,15 +929,10 @@ def main():
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/k/v, seeded trees/page tables/scores)",
         "config": config_dict(w, main_res["n_copies"]),
-        "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(kern_gbs / peak, 4), "traffic": profiled_traffic(args.config),
-                     "kernel": kernel_name, "kernel_us": round(kern_s * 1e6, 3),
-                     "kernel_us_from": "timed region / steps" if launches == 1 else "single-call CUDA events",
-                     "call_us": round(main_res["call_s"] * 1e6, 3),
-                     "call_us_p10_p50_p90": [round(x * 1e6, 3) for x in main_res["call_pct"]],
-                     "peak_kind": peak_kind},
+        "roofline": main_res["roofline"],
+        "sustained": main_res["sustained"],
         "e2e": main_res.get("e2e"),
-        "gpu_launches": main_res["steps"] * launches,
+        "gpu_launches": main_res["steps"] * main_res["launches"],
         "clocks": main_res["clocks"],
     }
     if "cpu" in main_res:
