@@ -568,6 +568,9 @@ def attention_path(w):
     if small_rows:
         nr = 16 if R <= 16 else (32 if R <= 32 else 64)
         kernel, launches = f"verify_attn_tck_kernel<{nr}> (keys on TMEM lanes, LSE merge inside)", 1
+    elif (w.dtype == "bf16" and w.D == 128 and R > 128 and os.environ.get("VA_MANY_ROWS_KERNEL") == "tcp"
+          and (w.layout == "dense" or (w.layout == "paged" and w.page_size >= 8))):
+        kernel, launches = "verify_attn_tcp_kernel (two M-tiles of rows on TMEM lanes, LSE merge inside)", 1
     elif w.dtype == "bf16" and w.D == 128:
         kernel, launches = "verify_attn_tc_kernel (rows on TMEM lanes) + split-segment merge kernel", 2
     else:

@@ -269,14 +269,6 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.test_drop_part = g_test_drop_part.load();
   if (const unsigned long long tw = g_test_wait_ns.load()) p.wait_ns = tw;
 
-  // key tiles an upper bound can produce; the grid never exceeds them
-  long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
-  const long long tile_keys = rp.use_tc == 2 ? 128 : 64;
-  const long long tiles_cap = (long long)rp.S * ((keys_cap + tile_keys - 1) / tile_keys);
-  if (tiles_cap >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "problem too large (%lld key tiles)", tiles_cap);
-  const long long ctas = (long long)rp.cps * sms;
-  const int grid = (int)(tiles_cap < ctas ? tiles_cap : ctas);
-  if (va::attn_smem_required(p) > 232448) return fail(VA_ERR_UNSUPPORTED, "shared memory plan too large");
   CUtensorMap tmk, tmv;
   memset(&tmk, 0, sizeof tmk);
   memset(&tmv, 0, sizeof tmv);
@@ -297,6 +289,21 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
         encode_cache_map(&tmv, v, s.dtype, s.D, s.Hkv, rows, box))
       p.tma_box = box;
   }
+  // more than 128 packed rows with K/V tiles by TMA: VA_MANY_ROWS_KERNEL=tcp
+  // selects the two-M-tile kernel of 128-key tiles instead of the 64-key
+  // rows-on-lanes kernel
+  if (p.use_tc == 1 && p.rows_pad == 256 && p.tma_box > 0) {
+    const char *e = getenv("VA_MANY_ROWS_KERNEL");
+    if (e != nullptr && strcmp(e, "tcp") == 0) p.use_tc = 3;
+  }
+  // key tiles an upper bound can produce; the grid never exceeds them
+  const long long keys_cap = (layout == VA_LAYOUT_SPARSE) ? (long long)max_indices + s.T : (long long)len_cap;
+  const long long tile_keys = p.use_tc >= 2 ? 128 : 64;
+  const long long tiles_cap = (long long)rp.S * ((keys_cap + tile_keys - 1) / tile_keys);
+  if (tiles_cap >= (1ll << 31)) return fail(VA_ERR_UNSUPPORTED, "problem too large (%lld key tiles)", tiles_cap);
+  const long long ctas = (long long)rp.cps * sms;
+  const int grid = (int)(tiles_cap < ctas ? tiles_cap : ctas);
+  if (va::attn_smem_required(p) > 232448) return fail(VA_ERR_UNSUPPORTED, "shared memory plan too large");
   cudaError_t e = va::launch_attention(p, tmk, tmv, grid < 1 ? 1 : grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok();

@@ -735,6 +735,7 @@ static cudaError_t launch_attn_t(const AttnParams &p, const CUtensorMap &tmk, co
 }
 
 size_t attn_smem_required(const AttnParams &p) {
+  if (p.use_tc == 3) return attn_tcp_smem_required(p);
   if (p.use_tc == 1) return attn_tc_smem_required(p);
   if (p.use_tc == 2) return attn_tck_smem_required(p);
   if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4, 1>(p.S);
@@ -750,6 +751,8 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
     e = launch_attention_tc(p, tmk, tmv, grid, stream);
   } else if (p.use_tc == 2) {
     return launch_attention_tck(p, tmk, tmv, grid, stream);  // merges its split segments itself
+  } else if (p.use_tc == 3) {
+    return launch_attention_tcp(p, tmk, tmv, grid, stream);  // merges its split segments itself
   } else if (p.dtype == VA_DTYPE_FP32) {
     e = launch_attn_t<float, 64, 4>(p, tmk, tmv, grid, stream);
   } else if (p.D == 64) {

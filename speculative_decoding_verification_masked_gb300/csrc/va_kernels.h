@@ -19,7 +19,9 @@ struct AttnParams {
   int S;       // segments = B * Hkv * NRB
   int rows_pad;// rows per segment slot in the partial buffers
   int use_tc;  // tcgen05 kernels (bf16, D 128): 1 = rows on TMEM lanes (more than 64
-              // packed rows), 2 = keys on TMEM lanes (at most 64); 0 = mma.sync kernel
+              // packed rows), 2 = keys on TMEM lanes (at most 64), 3 = rows on TMEM
+              // lanes, two M-tiles of 128-key TMA tiles (more than 128 rows, dense or
+              // paged with pages of 8 rows or more); 0 = mma.sync kernel
   int cps;     // CTAs of the attention kernel resident per SM (1 or 2)
   float scale;
   va_dtype dtype;
@@ -57,6 +59,10 @@ size_t attn_tc_smem_required(const AttnParams &p);
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream);
 size_t attn_tck_smem_required(const AttnParams &p);
+size_t attn_tcp_smem_required(const AttnParams &p);
+// the two-M-tile kernel merges its split segments itself (cooperative launch)
+cudaError_t launch_attention_tcp(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                 cudaStream_t stream);
 // the keys-on-lanes kernel merges split segments itself (cooperative launch)
 cudaError_t launch_attention_tck(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream);

@@ -213,6 +213,31 @@ def test_unread_cache_rows_poisoned(case):
     _check(_poison_unread_rows(w), "mask")
 
 
+@pytest.mark.parametrize("page_size", [8, 16, 64])
+@pytest.mark.parametrize("kernel", ["tcp", "tc"])
+def test_many_rows_paged_tma(page_size, kernel, monkeypatch):
+    """More than 128 packed rows over pages of 8 rows or more: one TMA box
+    per page into the two-M-tile kernel of 128-key tiles (VA_MANY_ROWS_KERNEL=tcp)
+    or the 64-key rows-on-lanes kernel."""
+    monkeypatch.setenv("VA_MANY_ROWS_KERNEL", kernel)
+    w = W.make_workload("paged", seed=50 + page_size, B=3, Hkv=2, Hq=8, T=40, L_lo=100, L_hi=2600,
+                        page_size=page_size, tree="depth", depth=5, spare_pages=3)
+    _check(_poison_unread_rows(w), "parent")
+
+
+@pytest.mark.parametrize("kernel", ["tcp", "tc"])
+def test_many_rows_both_kernels(kernel, monkeypatch):
+    """Both kernels for more than 128 dense rows: 144 rows (one row block,
+    the second M-tile partly padding), 640 rows (three row blocks), ragged
+    lengths with segments whole inside one CTA and cut over many."""
+    monkeypatch.setenv("VA_MANY_ROWS_KERNEL", kernel)
+    _check(W.make_workload("tree", seed=61, Hq=32, Hkv=2, T=9, D=128, L=5170, tree="random", B=2), "parent")
+    _check(W.make_workload("tree", seed=62, Hq=16, Hkv=1, T=40, D=128, L_lo=1, L_hi=3000, tree="random", B=3),
+           "parent")
+    _check(W.make_workload("tree", seed=63, B=5, Hkv=2, Hq=8, T=64, L_lo=0, L_hi=400, tree="random_mask",
+                           density=0.3), "mask")
+
+
 @pytest.mark.parametrize("layout", ["paged", "sparse"])
 def test_many_rows_through_gathers(layout):
     """More than 64 packed rows (rows on the TMEM lanes) with K/V rows gathered
@@ -422,6 +447,27 @@ def test_timeout_then_recovery():
         out, lse = run_library(w, "parent", workspace=ws)
         va.verify_attn_check_status(ws)
         compare(out, lse, oracle.verify(w), strict=True)
+
+
+def test_timeout_then_recovery_many_rows(monkeypatch):
+    """The same injected timeout in the two-M-tile kernel (tree workload shape,
+    two kv-heads): every segment is cut over many CTAs."""
+    monkeypatch.setenv("VA_MANY_ROWS_KERNEL", "tcp")
+    L = va.api.lib()
+    w = W.make_workload("tree", seed=206, Hkv=2, Hq=8, L=20000)
+    ws = va.Workspace.for_shape(va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0))
+    assert L.verify_attn_test_inject(2_000_000, 0) == 0
+    try:
+        run_library(w, "parent", workspace=ws)
+        with pytest.raises(va.VerifyAttnError) as ei:
+            va.verify_attn_check_status(ws)
+        assert ei.value.status == va.api.VA_ERR_TIMEOUT
+    finally:
+        assert L.verify_attn_test_inject(0, -1) == 0
+    assert L.verify_attn_workspace_init(ws.ptr, ws.nbytes, va.api._stream()) == 0
+    out, lse = run_library(w, "parent", workspace=ws)
+    va.verify_attn_check_status(ws)
+    compare(out, lse, oracle.verify(w), strict=True)
 
 
 def test_workspace_too_small_is_rejected():

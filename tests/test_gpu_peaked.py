@@ -84,6 +84,14 @@ def test_sink_dominated_rows_mma_route(monkeypatch):
     _run(w, "parent")
 
 
+def test_sink_dominated_rows_two_mtile_kernel(monkeypatch):
+    """More than 128 rows on the two-M-tile kernel of 128-key tiles (VA_MANY_ROWS_KERNEL=tcp)."""
+    monkeypatch.setenv("VA_MANY_ROWS_KERNEL", "tcp")
+    w = W.make_workload("tree", seed=92, B=1, Hkv=2, Hq=8, L=3000)
+    _run.sinks = make_peaked(w, n_sinks=5, seed=6)
+    _run(w, "parent")
+
+
 @pytest.mark.parametrize("n_sinks", [2, 9, 16])
 def test_sink_count(n_sinks):
     """Two sinks (one of them key 0), and many: on the rows-on-lanes kernel a
