@@ -307,6 +307,71 @@ def measure_rope(va, peak, steps=1024):
             "note": "about 21 MB a call: launch- and latency-bound, the rows mostly served from L2 in the loop"}
 
 
+def measure_rope_fused(va, peak, steps=512):
+    """The rotary embedding inside the attention kernels against the separate
+    pass: at the paged and chain workloads' shapes, one step of (rotation pass
+    + unrotated attention) against one attention call given the positions
+    (tree / chain positions L + depth, base 500000).  Device time per step from
+    CUDA events around graphs of 32 steps over resident input copies larger
+    than L2."""
+    res = {}
+    for name in ("paged", "chain"):
+        w = W.make_workload(name, seed=0)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.int32))).cuda()  # noqa: E731
+        depth = (np.stack([W.chain_depths(p) for p in w.parent]) if w.parent is not None
+                 else np.tile(np.arange(w.T, dtype=np.int32), (w.B, 1)))
+        pos = i32(w.seqlens[:, None] + depth)
+        cases = [DeviceCase(w, va) for _ in range(n_copies_for(w))]
+
+        def sep(c):
+            if w.layout == "paged":
+                va.verify_rope_draft_paged(c.q, c.k, c.page_table, c.seqlens, pos, 500000.0)
+            else:
+                va.verify_rope_draft_dense(c.q, c.k, c.seqlens, pos, 500000.0)
+            c.step()
+
+        def fused(c):
+            if w.layout == "paged":
+                va.verify_attn_paged(c.q, c.k, c.v, c.page_table, c.seqlens, tree_parent=c.parent, tree_mask=c.mask,
+                                     positions=pos, rope_base=500000.0, out=c.out, lse=c.lse, workspace=c.ws,
+                                     scale=w.scale)
+            else:
+                va.verify_attn_dense(c.q, c.k, c.v, c.seqlens, tree_parent=c.parent, tree_mask=c.mask,
+                                     positions=pos, rope_base=500000.0, out=c.out, lse=c.lse, workspace=c.ws,
+                                     scale=w.scale)
+
+        out = {}
+        for tag, fn in (("rotation_pass_then_attention_us", sep), ("attention_with_rotation_inside_us", fused),
+                        ("attention_without_rotation_us", lambda c: c.step())):
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for c in cases:
+                    fn(c)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(32):
+                    fn(cases[i % len(cases)])
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = max(1, steps // 32)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            out[tag] = round(e0.elapsed_time(e1) * 1e3 / (reps * 32), 3)
+            del g
+        for c in cases:
+            va.verify_attn_check_status(c.ws)
+        res[name] = out
+        del cases
+        torch.cuda.empty_cache()
+    return res
+
+
 def measure_scoring(va, peak, steps=256):
     """The importance pass of a few query heads at the sparse workload's shape
     (B16, T5, Hq32/Hkv8, prefixes 16K-32K, two synthetic retrieval heads on
@@ -911,6 +976,7 @@ def main():
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
     rope = measure_rope(va, peak) if args.all_configs and rank == 0 else None
+    rope_fused = measure_rope_fused(va, peak) if args.all_configs and rank == 0 else None
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -948,6 +1014,8 @@ def main():
         line["scoring_pass"] = scoring
     if rope is not None:
         line["rope_draft"] = rope
+    if rope_fused is not None:
+        line["rope_inside_attention"] = rope_fused
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

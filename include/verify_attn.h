@@ -41,6 +41,19 @@
  * Draft keys.  The T draft tokens' keys and values are already in the cache at
  *   logical slots L_b .. L_b+T-1 (append, then verify; rejected entries are
  *   dropped afterwards).
+ * Rotary embedding (LongSpec section 1: the target keeps its own RoPE base;
+ *   position ids may be arbitrary, e.g. anchor-offset ids).  With positions ==
+ *   NULL the attention calls take q and the draft keys as stored (already
+ *   rotated, e.g. by verify_rope_draft_*).  With positions != NULL they rotate
+ *   q and the T draft keys on the fly, inside the attention kernels, exactly
+ *   as verify_rope_draft_* would (rotate-half layout, element i with i + D/2,
+ *   angle positions[b][t] * rope_base^(-2i/D), reduced modulo 2 pi to ~5e-7
+ *   rad), and write neither q nor the cache; the prefix keys are taken as
+ *   stored.  Requires shape->rope_base > 0 and |positions| < 2^24 (a larger
+ *   one is recorded as VA_ERR_DEVICE_BOUNDS and taken as 0).  The accepted
+ *   draft keys stay unrotated in the cache: once verify_commit_kv_* has moved
+ *   them to L_b .. L_b+a-1, verify_rope_draft_* at the accepted tokens'
+ *   positions rotates them for the next step (for a tree, L_b + depth).
  * GQA.  Query head h reads kv head h / (Hq/Hkv).
  * Draft visibility.  Exactly one of tree_parent / tree_mask may be non-NULL.
  *   With tree_parent, token i sees itself and its ancestors (computed inside
@@ -94,6 +107,8 @@ typedef struct {
   int D;         /* head dimension */
   va_dtype dtype;/* element type of q, k, v and out */
   float scale;   /* score scale (1/sqrt(D) for standard attention) */
+  float rope_base; /* RoPE base of the model, read only when an attention call
+                    * is given positions (see "Rotary embedding" below) */
 } va_shape;
 
 /* Bytes of workspace the attention calls need for `shape` on the CURRENT
@@ -109,9 +124,9 @@ va_status verify_attn_workspace_init(void *workspace, size_t ws_bytes, va_stream
  * LongSpec section 2.C: unmasked split-KV pass over the L_b cached keys
  * (FlashAttention-style, no mask), masked pass over the T draft keys at slots
  * L_b..L_b+T-1, exact log-sum-exp merge.  Requires L_b + T <= max_cache_len
- * (checked on the device).  positions may be NULL and is not read: q and k
- * must already carry their positional rotation (verify_rope_draft_dense /
- * _paged rotates q and the draft keys in one launch before this call).
+ * (checked on the device).  positions: NULL, or [B][T] int32 position ids
+ * of the draft tokens to rotate q and the draft keys on the fly (see "Rotary
+ * embedding" above; verify_rope_draft_* is the separate pass).
  */
 va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_cache,
                             const void *v_cache, int max_cache_len, const int32_t *seqlens,

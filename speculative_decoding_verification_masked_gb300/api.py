@@ -32,7 +32,8 @@ class VerifyAttnError(RuntimeError):
 
 class VaShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
-                ("D", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("D", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
+                ("rope_base", ctypes.c_float)]
 
 
 _lock = threading.Lock()
@@ -124,10 +125,10 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported element type {t.dtype}; use bfloat16 or float32")
 
 
-def make_shape(B, T, Hq, Hkv, D, dtype_code, scale=None) -> VaShape:
+def make_shape(B, T, Hq, Hkv, D, dtype_code, scale=None, rope_base=0.0) -> VaShape:
     if scale is None:
         scale = 1.0 / float(D) ** 0.5
-    return VaShape(int(B), int(T), int(Hq), int(Hkv), int(D), int(dtype_code), float(scale))
+    return VaShape(int(B), int(T), int(Hq), int(Hkv), int(D), int(dtype_code), float(scale), float(rope_base))
 
 
 def workspace_size(shape: VaShape) -> int:
@@ -161,9 +162,9 @@ class Workspace:
 # entry points (same names as the C ABI)
 # ----------------------------------------------------------------------------
 
-def _shape_of(q, Hkv, scale):
+def _shape_of(q, Hkv, scale, rope_base=0.0):
     B, T, Hq, D = q.shape
-    return make_shape(B, T, Hq, Hkv, D, _dtype_code(q), scale)
+    return make_shape(B, T, Hq, Hkv, D, _dtype_code(q), scale, rope_base)
 
 
 def _outputs(q, out, lse):
@@ -176,9 +177,11 @@ def _outputs(q, out, lse):
 
 
 def verify_attn_dense(q, k_cache, v_cache, seqlens, tree_parent=None, tree_mask=None, positions=None,
-                      out=None, lse=None, workspace: Workspace = None, scale=None, stream=None):
-    """Dense-cache verification attention; returns (out [B][T][Hq][D], lse [B][Hq][T])."""
-    shape = _shape_of(q, k_cache.shape[2], scale)
+                      out=None, lse=None, workspace: Workspace = None, scale=None, stream=None, rope_base=0.0):
+    """Dense-cache verification attention; returns (out [B][T][Hq][D], lse [B][Hq][T]).
+    With positions [B][T] int32 (and rope_base > 0) q and the draft keys are
+    rotated inside the kernels."""
+    shape = _shape_of(q, k_cache.shape[2], scale, rope_base)
     out, lse = _outputs(q, out, lse)
     ws = workspace or Workspace.for_shape(shape, q.device, stream)
     _check(lib().verify_attn_dense(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[1],
@@ -188,10 +191,10 @@ def verify_attn_dense(q, k_cache, v_cache, seqlens, tree_parent=None, tree_mask=
 
 
 def verify_attn_dense_noalloc(q, k_cache, v_cache, seqlens, tree_parent=None, tree_mask=None, positions=None,
-                              out=None, lse=None, device_status=None, scale=None, stream=None):
+                              out=None, lse=None, device_status=None, scale=None, stream=None, rope_base=0.0):
     """verify_attn_dense without a workspace (fixed 8 MiB static device scratch inside
     the library) for callers that cannot allocate; see include/verify_attn.h."""
-    shape = _shape_of(q, k_cache.shape[2], scale)
+    shape = _shape_of(q, k_cache.shape[2], scale, rope_base)
     out, lse = _outputs(q, out, lse)
     _check(lib().verify_attn_dense_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                            k_cache.shape[1], _ptr(seqlens), _ptr(tree_parent), _ptr(tree_mask),
@@ -201,9 +204,9 @@ def verify_attn_dense_noalloc(q, k_cache, v_cache, seqlens, tree_parent=None, tr
 
 
 def verify_attn_paged(q, k_pages, v_pages, page_table, seqlens, tree_parent=None, tree_mask=None, positions=None,
-                      out=None, lse=None, workspace: Workspace = None, scale=None, stream=None):
+                      out=None, lse=None, workspace: Workspace = None, scale=None, stream=None, rope_base=0.0):
     """Paged-cache verification attention; pages [P][page][Hkv][D], page_table int32 [B][max_pages]."""
-    shape = _shape_of(q, k_pages.shape[2], scale)
+    shape = _shape_of(q, k_pages.shape[2], scale, rope_base)
     out, lse = _outputs(q, out, lse)
     ws = workspace or Workspace.for_shape(shape, q.device, stream)
     _check(lib().verify_attn_paged(ctypes.byref(shape), _ptr(q), _ptr(k_pages), _ptr(v_pages), k_pages.shape[0],
@@ -214,9 +217,10 @@ def verify_attn_paged(q, k_pages, v_pages, page_table, seqlens, tree_parent=None
 
 
 def verify_attn_sparse(q, k_cache, v_cache, seqlens, indices, n_indices, tree_parent=None, tree_mask=None,
-                       positions=None, out=None, lse=None, workspace: Workspace = None, scale=None, stream=None):
+                       positions=None, out=None, lse=None, workspace: Workspace = None, scale=None, stream=None,
+                       rope_base=0.0):
     """Sparse verification over per-(sequence, kv-head) verify index sets [B][Hkv][max_indices]."""
-    shape = _shape_of(q, k_cache.shape[2], scale)
+    shape = _shape_of(q, k_cache.shape[2], scale, rope_base)
     out, lse = _outputs(q, out, lse)
     ws = workspace or Workspace.for_shape(shape, q.device, stream)
     _check(lib().verify_attn_sparse(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[1],

@@ -185,6 +185,7 @@ struct Common {
   const void *q;
   const int32_t *seqlens, *parent;
   const uint32_t *mask;
+  const int32_t *positions;
   void *out;
   float *lse;
   void *ws;
@@ -198,6 +199,8 @@ va_status check_common(const Common &c) {
     return fail(VA_ERR_INVALID_ARG, "q, seqlens, out and lse must not be NULL");
   if (c.parent != nullptr && c.mask != nullptr)
     return fail(VA_ERR_INVALID_ARG, "give tree_parent or tree_mask, not both");
+  if (c.positions != nullptr && (!(c.shape->rope_base > 0.f) || !isfinite(c.shape->rope_base)))
+    return fail(VA_ERR_INVALID_ARG, "rotating on the fly (positions given) needs shape->rope_base > 0");
   const size_t el = c.shape->dtype == VA_DTYPE_BF16 ? 2 : 4;
   const size_t out_align = el == 2 ? 8 : 4;
   if (!aligned(c.q, 16) || !aligned(c.out, out_align))
@@ -252,6 +255,14 @@ va_status run_attention(const Common &c, int layout, const void *k, const void *
   p.parent = c.parent;
   p.mask = c.mask;
   p.mask_words = (s.T + 31) / 32;
+  p.positions = c.positions;
+  if (c.positions != nullptr) {
+    for (int i = 0; i < s.D / 2; ++i) {
+      const double f = pow((double)s.rope_base, -(double)(2 * i) / s.D);
+      p.rope_fhi[i] = (float)f;
+      p.rope_flo[i] = (float)(f - (double)p.rope_fhi[i]);
+    }
+  }
   p.out = c.out;
   p.out_align16 = aligned(c.out, 16) ? 1 : 0;
   p.lse = c.lse;
@@ -400,8 +411,7 @@ va_status verify_attn_dense(const va_shape *shape, const void *q, const void *k_
                             int max_cache_len, const int32_t *seqlens, const int32_t *tree_parent,
                             const uint32_t *tree_mask, const int32_t *positions, void *out, float *lse,
                             void *workspace, size_t ws_bytes, va_stream stream) {
-  (void)positions;
-  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  Common c{shape, q, seqlens, tree_parent, tree_mask, positions, out, lse, workspace, ws_bytes};
   va_status st = check_common(c);
   if (st != VA_OK) return st;
   if (k_cache == nullptr || v_cache == nullptr) return fail(VA_ERR_INVALID_ARG, "k_cache and v_cache must not be NULL");
@@ -417,8 +427,7 @@ va_status verify_attn_paged(const va_shape *shape, const void *q, const void *k_
                             const int32_t *seqlens, const int32_t *tree_parent, const uint32_t *tree_mask,
                             const int32_t *positions, void *out, float *lse, void *workspace, size_t ws_bytes,
                             va_stream stream) {
-  (void)positions;
-  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  Common c{shape, q, seqlens, tree_parent, tree_mask, positions, out, lse, workspace, ws_bytes};
   va_status st = check_common(c);
   if (st != VA_OK) return st;
   if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr)
@@ -439,8 +448,7 @@ va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k
                              const int32_t *n_indices, int max_indices, const int32_t *tree_parent,
                              const uint32_t *tree_mask, const int32_t *positions, void *out, float *lse,
                              void *workspace, size_t ws_bytes, va_stream stream) {
-  (void)positions;
-  Common c{shape, q, seqlens, tree_parent, tree_mask, out, lse, workspace, ws_bytes};
+  Common c{shape, q, seqlens, tree_parent, tree_mask, positions, out, lse, workspace, ws_bytes};
   va_status st = check_common(c);
   if (st != VA_OK) return st;
   if (k_cache == nullptr || v_cache == nullptr || indices == nullptr || n_indices == nullptr)

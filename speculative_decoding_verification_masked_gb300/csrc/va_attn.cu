@@ -36,6 +36,7 @@
 #include "va_common.cuh"
 #include "va_kernels.h"
 #include "va_pipeline.cuh"
+#include "va_rope_fused.cuh"
 
 namespace va {
 
@@ -57,7 +58,7 @@ struct Cfg : StageGeom<Tin, D> {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <typename Tin, int D, int RG, int CPS>
+template <typename Tin, int D, int RG, int CPS, bool kRope>
 __global__ void __launch_bounds__(kThreads, CPS)
     verify_attn_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
@@ -75,6 +76,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
   uint64_t *empty = full + NS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NS);
   int *tstart = reinterpret_cast<int *>(empty + NS) + 4;
+  // the rotary table of the segment (when positions are given), after the plan
+  float2 *rope_tab = reinterpret_cast<float2 *>(tstart + ((p.S + 1 + 3) & ~3));
+  constexpr int kBarRope = 2;  // consumer warps only
   const bool use_tma = p.tma_box > 0;
 
   const int tid = threadIdx.x;
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
   const int group = p.Hq / p.Hkv;
   int it = 0;
   bool ok = true;
+  int rope_b = -1;  // sequence whose rotary table is in shared memory
 
   for (int s = s0; s < S && tstart[s] < t1; ++s) {
     const Seg g = seg_info(p, s, false);
@@ -127,6 +132,24 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const bool has_draft = lt1 * kTK > g.n_prefix;
     uint64_t tl = 0, th = 0;
     if (has_draft && p.parent != nullptr) warp_tree_rows(p, g.b, tl, th);
+    if (kRope && g.b != rope_b) {
+      // rotary table of this sequence's draft tokens, kept while the CTA stays
+      // on the sequence (the previous segment's readers are past the barrier first)
+      named_bar_sync(kBarRope, kNWC * 32);
+      rope_build_table(p, g.b, rope_tab, tid, kNWC * 32);
+      named_bar_sync(kBarRope, kNWC * 32);
+      rope_b = g.b;
+    }
+    // the draft keys of tile lt, rotated in place by the consumer warps together
+    // before any of them reads the tile
+    auto rotate_draft = [&](int lt, int st) {
+      if (!kRope || lt * kTK + kTK <= g.n_prefix) return;
+      named_bar_sync(kBarRope, kNWC * 32);
+      const int r0 = max(0, g.n_prefix - lt * kTK), r1 = min(kTK, g.nkeys - lt * kTK);
+      rope_rotate_tile_rows<Tin, D, kTK>(stages + st * C::kStageBytes, r0, r1, lt * kTK + r0 - g.n_prefix, rope_tab,
+                                         tid, kNWC * 32);
+      named_bar_sync(kBarRope, kNWC * 32);
+    };
 
     if constexpr (!C::kF32) {
       // ------------------------- bf16 tensor-core path -------------------------
@@ -166,6 +189,22 @@ __global__ void __launch_bounds__(kThreads, CPS)
           qa[ks][2] = rvalid[0] ? __ldg(qrow[0] + ks * 8 + 4 + tq) : 0u;
           qa[ks][3] = rvalid[1] ? __ldg(qrow[1] + ks * 8 + 4 + tq) : 0u;
         }
+        if constexpr (kRope) {
+          // each fragment register holds columns e, e+1 of one row; its partners
+          // e + D/2, e+1 + D/2 sit in the fragment D/32 k-steps further
+#pragma unroll
+          for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int h = j & 1;
+              const int e = ks * 16 + (j >> 1) * 8 + 2 * tq;
+              const float2 *cs = rope_tab + trow[h] * (D / 2) + e;
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[ks][j]));
+              const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qa[ks + D / 32][j]));
+              qa[ks][j] = pack_bf16(x.x * cs[0].x - y.x * cs[0].y, x.y * cs[1].x - y.y * cs[1].y);
+              qa[ks + D / 32][j] = pack_bf16(y.x * cs[0].x + x.x * cs[0].y, y.y * cs[1].x + x.y * cs[1].y);
+            }
+        }
       }
       float o[D / 8][4];
 #pragma unroll
@@ -182,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
           *abort_flag = 1;
           ok = false;
         }
+        rotate_draft(lt, st);
         if (ok) {
           const uint32_t ks_addr = smem_u32(stages + st * C::kStageBytes);
           const uint32_t vs_addr = ks_addr + C::kTileBytes;
@@ -403,6 +443,15 @@ __global__ void __launch_bounds__(kThreads, CPS)
           qv[4 * i + 2] = v4.z;
           qv[4 * i + 3] = v4.w;
         }
+        if constexpr (kRope) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 cs = rope_tab[t * 32 + i];
+            const float x = qv[i], y = qv[i + 32];
+            qv[i] = x * cs.x - y * cs.y;
+            qv[i + 32] = y * cs.x + x * cs.y;
+          }
+        }
       }
       float o[64];
 #pragma unroll
@@ -417,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
           *abort_flag = 1;
           ok = false;
         }
+        rotate_draft(lt, st);
         if (ok) {
           const uint8_t *kt = stages + st * C::kStageBytes;
           uint8_t *vt = stages + st * C::kStageBytes + C::kTileBytes;
@@ -717,17 +767,19 @@ __global__ void __launch_bounds__(128) combine_generic_kernel(int n_rows, int n_
 // host-side launch helpers
 // ---------------------------------------------------------------------------
 template <typename Tin, int D, int RG, int CPS>
-static size_t attn_smem_bytes(int S) {
+static size_t attn_smem_bytes(const AttnParams &p) {
   using C = Cfg<Tin, D, CPS>;
   return 1024 + (size_t)C::kStages * C::kStageBytes + C::kMergeBytes + 2 * C::kStages * 8 + 16 +
-         (size_t)(S + 1) * 4;
+         (size_t)((p.S + 1 + 3) & ~3) * 4 + (size_t)rope_table_bytes(p);
 }
 
 template <typename Tin, int D, int RG, int CPS = 1>
 static cudaError_t launch_attn_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream) {
-  const size_t smem = attn_smem_bytes<Tin, D, RG, CPS>(p.S);
-  auto kern = verify_attn_kernel<Tin, D, RG, CPS>;
+  const size_t smem = attn_smem_bytes<Tin, D, RG, CPS>(p);
+  // instances with and without the rotary embedding (code that never runs
+  // still costs the hot loop)
+  auto kern = p.positions != nullptr ? verify_attn_kernel<Tin, D, RG, CPS, true> : verify_attn_kernel<Tin, D, RG, CPS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(p, tmk, tmv);
@@ -738,10 +790,10 @@ size_t attn_smem_required(const AttnParams &p) {
   if (p.use_tc == 3) return attn_tcp_smem_required(p);
   if (p.use_tc == 1) return attn_tc_smem_required(p);
   if (p.use_tc == 2) return attn_tck_smem_required(p);
-  if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4, 1>(p.S);
-  if (p.cps == 2) return p.D == 64 ? attn_smem_bytes<__nv_bfloat16, 64, 2, 2>(p.S) : attn_smem_bytes<__nv_bfloat16, 128, 2, 2>(p.S);
-  if (p.D == 64) return attn_smem_bytes<__nv_bfloat16, 64, 4, 1>(p.S);
-  return attn_smem_bytes<__nv_bfloat16, 128, 4, 1>(p.S);
+  if (p.dtype == VA_DTYPE_FP32) return attn_smem_bytes<float, 64, 4, 1>(p);
+  if (p.cps == 2) return p.D == 64 ? attn_smem_bytes<__nv_bfloat16, 64, 2, 2>(p) : attn_smem_bytes<__nv_bfloat16, 128, 2, 2>(p);
+  if (p.D == 64) return attn_smem_bytes<__nv_bfloat16, 64, 4, 1>(p);
+  return attn_smem_bytes<__nv_bfloat16, 128, 4, 1>(p);
 }
 
 cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,

@@ -42,6 +42,7 @@
 #include "va_common.cuh"
 #include "va_kernels.h"
 #include "va_pipeline.cuh"
+#include "va_rope_fused.cuh"
 #include "va_tcgen05.cuh"
 
 namespace va {
@@ -61,7 +62,9 @@ struct TcSmem {
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kLoFlagOff = kMiscOff + 16;          // int [2][2]: P residual written, per M-tile and buffer
-  static constexpr int kTstartOff = kLoFlagOff + 16;
+  // then the rotary table of the segment (rope_table_bytes, 0 without
+  // positions) and the tile starts of the work plan
+  static constexpr int kRopeOff = kLoFlagOff + 16;
   static constexpr int kThreads = (5 * NMT + 2) * 32;
 };
 
@@ -70,7 +73,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int NMT, bool kTma>
+template <int NMT, bool kTma, bool kRope>
 __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     verify_attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
@@ -97,7 +100,8 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint64_t *drain = bars + 2 * NS + 12;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
-  int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  float2 *rope_tab = reinterpret_cast<float2 *>(smem + SM::kRopeOff);
+  int *tstart = reinterpret_cast<int *>(smem + SM::kRopeOff + (kRope ? rope_table_bytes(p) : 0));
   volatile int *lo_flag = reinterpret_cast<volatile int *>(smem + SM::kLoFlagOff);
   constexpr bool use_tma = kTma;  // tiles by TMA boxes (dense, paged), else cp.async gathers
 
@@ -228,7 +232,17 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
           // S(t) of each M-tile into buffer b once PV(t-2) has read P from it
           for (int i = 0; i < NMT; ++i) {
             if (jt >= 2) wait_ok(o_done + 2 * i + b, (uint32_t)((jt - 2) >> 1) & 1u);
-            if (i == 0) wait_ok(full + st, (uint32_t)(it / NS) & 1u);
+            if (i == 0) {
+              wait_ok(full + st, (uint32_t)(it / NS) & 1u);
+              if (kRope && ok && lt * kTK + kTK > g.n_prefix) {
+                // the draft keys of this tile, rotated in place before the S MMAs read them
+                const int r0 = max(0, g.n_prefix - lt * kTK), r1 = min(kTK, g.nkeys - lt * kTK);
+                rope_rotate_tile_rows<__nv_bfloat16, D, kTK>(stages + st * Geo::kStageBytes, r0, r1,
+                                                             lt * kTK + r0 - g.n_prefix, rope_tab, lane, 32);
+                fence_proxy_async_smem();
+                __syncwarp();
+              }
+            }
             tc_fence_after();
             issue_s(i, b, st);
           }
@@ -268,6 +282,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     }
   };
   int jt = 0;
+  int rope_b = -1;  // sequence whose rotary table is in shared memory
   for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
     const Seg g = seg_info(p, s, false);
     const int lt0 = max(tstart[s], t0) - tstart[s];
@@ -282,7 +297,34 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 
     // ---- Q of this segment into shared memory (both warpgroups) ----
     named_bar_sync(kBarSoft, kSoftThreads);  // previous segment's MMAs have all completed
-    {
+    if constexpr (kRope) {
+      // rotary table of this sequence's draft tokens (kept while the CTA stays
+      // on the sequence), then q rotated on its way in
+      if (g.b != rope_b) {
+        rope_build_table(p, g.b, rope_tab, tid, kSoftThreads);
+        named_bar_sync(kBarSoft, kSoftThreads);
+        rope_b = g.b;
+      }
+      const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+      for (int e = tid; e < NMT * 128 * 8; e += kSoftThreads) {
+        const int m = e / (128 * 8);
+        const int row = (e / 8) % 128;
+        const int ch = e % 8;
+        const int rr = g.rb * p.rows_pad + m * 128 + row;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (rr < p.R) {
+          const int t = rr / group;
+          const int hq = g.hkv * group + rr % group;
+          const uint4 *src = reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D);
+          lo = __ldg(src + ch);
+          hi = __ldg(src + ch + 8);
+          rope_rotate8_bf16(lo, hi, rope_tab + t * (D / 2) + ch * 8);
+        }
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch)) = lo;
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch + 8)) = hi;
+      }
+      fence_proxy_async_smem();
+    } else {
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
       for (int e = tid; e < NMT * 128 * 16; e += kSoftThreads) {
         const int m = e / (128 * 16);
@@ -469,19 +511,21 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 template <int NMT>
-static size_t tc_smem_bytes(int S) {
-  return 1024 + (size_t)TcSmem<NMT>::kTstartOff + (size_t)(S + 1) * 4;
+static size_t tc_smem_bytes(const AttnParams &p) {
+  return 1024 + (size_t)TcSmem<NMT>::kRopeOff + (size_t)rope_table_bytes(p) + (size_t)(p.S + 1) * 4;
 }
 
 size_t attn_tc_smem_required(const AttnParams &p) {
-  return p.rows_pad > 128 ? tc_smem_bytes<2>(p.S) : tc_smem_bytes<1>(p.S);
+  return p.rows_pad > 128 ? tc_smem_bytes<2>(p) : tc_smem_bytes<1>(p);
 }
 
 template <int NMT, bool kTma>
 static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                cudaStream_t stream) {
-  const size_t smem = tc_smem_bytes<NMT>(p.S);
-  auto kern = verify_attn_tc_kernel<NMT, kTma>;
+  const size_t smem = tc_smem_bytes<NMT>(p);
+  // instances with and without the rotary embedding (code that never runs
+  // still costs the hot loop)
+  auto kern = p.positions != nullptr ? verify_attn_tc_kernel<NMT, kTma, true> : verify_attn_tc_kernel<NMT, kTma, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, TcSmem<NMT>::kThreads, smem, stream>>>(p, tmk, tmv);

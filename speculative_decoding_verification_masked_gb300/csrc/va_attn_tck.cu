@@ -46,6 +46,7 @@
 #include "va_kernels.h"
 #include "va_pipeline.cuh"
 #include "va_merge.cuh"
+#include "va_rope_fused.cuh"
 #include "va_tcgen05.cuh"
 
 namespace va {
@@ -76,7 +77,9 @@ struct TkSmem {
   static constexpr int kKeyMaskOff = kRowMaskOff + 512;    // u64 [64]: per draft key, rows that see it
   static constexpr int kRedOff = kKeyMaskOff + 512;        // float4 [NR]: per-warp row maxima
   static constexpr int kRowInvOff = kRedOff + NR * 16;     // float [64]: 1 / l per row (epilogue)
-  static constexpr int kTstartOff = kRowInvOff + 256;
+  // then the rotary table of the segment (rope_table_bytes, 0 without
+  // positions) and the tile starts of the work plan
+  static constexpr int kRopeOff = kRowInvOff + 256;
   static_assert(kQOff % 1024 == 0 && kQBytes % 1024 == 0, "UMMA operands need 1024-byte aligned swizzle atoms");
   static_assert(kBarOff % 8 == 0 && kRowMaskOff % 8 == 0 && kKeyMaskOff % 8 == 0, "8-byte alignment");
   static_assert(kRedOff % 16 == 0, "float4 array needs 16-byte alignment");
@@ -200,7 +203,7 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, const float *a) 
   }
 }
 
-template <int NR, bool kTma>
+template <int NR, bool kTma, bool kRope>
 __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     verify_attn_tck_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv) {
@@ -233,7 +236,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
   uint64_t *keymask = reinterpret_cast<uint64_t *>(smem + SM::kKeyMaskOff);
   float4 *red = reinterpret_cast<float4 *>(smem + SM::kRedOff);
   float *row_inv = reinterpret_cast<float *>(smem + SM::kRowInvOff);
-  int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  float2 *rope_tab = reinterpret_cast<float2 *>(smem + SM::kRopeOff);
+  int *tstart = reinterpret_cast<int *>(smem + SM::kRopeOff + (kRope ? rope_table_bytes(p) : 0));
   constexpr bool use_tma = kTma;  // tiles by TMA boxes (dense, paged), else cp.async gathers
 
   const int tid = threadIdx.x;
@@ -309,7 +313,15 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     // 16 KB apart
     const uint64_t dP0 = umma_sdesc(smem_u32(stages), TK * 128, 1024);
     constexpr uint64_t kStageStep = SM::kStageBytes >> 4;
-    auto issue_s = [&](int b, int st) {  // S^T(b) = K Q^T
+    auto issue_s = [&](int b, int st, const Seg &g, int lt) {  // S^T(b) = K Q^T
+      if (kRope && ok && lt * TK + TK > g.n_prefix) {
+        // the draft keys of this tile, rotated in place before the MMA reads them
+        const int r0 = max(0, g.n_prefix - lt * TK), r1 = min(TK, g.nkeys - lt * TK);
+        rope_rotate_tile_rows<__nv_bfloat16, D, TK>(stages + st * SM::kStageBytes, r0, r1, lt * TK + r0 - g.n_prefix,
+                                                    rope_tab, lane, 32);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (!ok || lane != 0) return;
       tc_fence_after();
       const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
@@ -345,10 +357,10 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoft + 32);  // Q of this segment is in shared memory
       wait_ok(full + it % NS, (uint32_t)(it / NS) & 1u);
-      issue_s(jt & 1, it % NS);
+      issue_s(jt & 1, it % NS, g, lt0);
       if (lt0 + 1 < lt1) {
         wait_ok(full + (it + 1) % NS, (uint32_t)((it + 1) / NS) & 1u);
-        issue_s((jt + 1) & 1, (it + 1) % NS);
+        issue_s((jt + 1) & 1, (it + 1) % NS, g, lt0 + 1);
       }
       for (int lt = lt0; lt < lt1; ++lt, ++it, ++jt) {
         const int b = jt & 1;
@@ -356,7 +368,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         issue_pv(it % NS, b, lt == lt0);
         if (lt + 2 < lt1) {
           wait_ok(full + (it + 2) % NS, (uint32_t)((it + 2) / NS) & 1u);
-          issue_s(b, (it + 2) % NS);
+          issue_s(b, (it + 2) % NS, g, lt + 2);
         }
         __syncwarp();
       }
@@ -383,6 +395,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     tmem_st_wait();
   }
   int it = 0, jt = 0;
+  int rope_b = -1;  // sequence whose rotary table is in shared memory
   // split segments this CTA holds a part of (at most its first and its last):
   // merged after its last tile
   int n_split = 0, ms[2] = {0, 0}, mslot[2] = {0, 0}, mnp[2] = {0, 0}, mpart[2] = {0, 0};
@@ -396,7 +409,31 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 
     // ---- Q of this segment into shared memory: [2 columns][NR rows][128 B], 128B swizzle ----
     // (the previous segment's MMAs have completed: its epilogue waited for the last one)
-    {
+    if constexpr (kRope) {
+      // rotary table of this sequence's draft tokens (kept while the CTA stays
+      // on the sequence), then q rotated on its way in
+      if (g.b != rope_b) {
+        rope_build_table(p, g.b, rope_tab, tid, kSoft);
+        named_bar_sync(kBarSoft, kSoft);
+        rope_b = g.b;
+      }
+      const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+      for (int e = tid; e < NR * 8; e += kSoft) {
+        const int row = e >> 3, ch = e & 7;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (row < p.R) {
+          const int t = row / group;
+          const int hq = g.hkv * group + row % group;
+          const uint4 *src = reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D);
+          lo = __ldg(src + ch);
+          hi = __ldg(src + ch + 8);
+          rope_rotate8_bf16(lo, hi, rope_tab + t * (D / 2) + ch * 8);
+        }
+        *reinterpret_cast<uint4 *>(sQ + row * 128 + ((ch ^ (row & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(sQ + NR * 128 + row * 128 + ((ch ^ (row & 7)) << 4)) = hi;
+      }
+      fence_proxy_async_smem();
+    } else {
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
       for (int e = tid; e < NR * 16; e += kSoft) {
         const int row = e >> 4, ch = e & 15;
@@ -771,20 +808,22 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 template <int NR>
-static size_t tck_smem_bytes(int S) {
-  return 1024 + (size_t)TkSmem<NR>::kTstartOff + (size_t)(S + 1) * 4;
+static size_t tck_smem_bytes(const AttnParams &p) {
+  return 1024 + (size_t)TkSmem<NR>::kRopeOff + (size_t)rope_table_bytes(p) + (size_t)(p.S + 1) * 4;
 }
 
+// A kernel instance with the rotary embedding and one without: code that never
+// runs still costs the hot loop registers and schedule.
+
 size_t attn_tck_smem_required(const AttnParams &p) {
-  return p.rows_pad <= 16 ? tck_smem_bytes<16>(p.S) : p.rows_pad <= 32 ? tck_smem_bytes<32>(p.S)
-                                                                       : tck_smem_bytes<64>(p.S);
+  return p.rows_pad <= 16 ? tck_smem_bytes<16>(p) : p.rows_pad <= 32 ? tck_smem_bytes<32>(p) : tck_smem_bytes<64>(p);
 }
 
 template <int NR, bool kTma>
 static cudaError_t launch_tck_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                 cudaStream_t stream) {
-  const size_t smem = tck_smem_bytes<NR>(p.S);
-  auto kern = verify_attn_tck_kernel<NR, kTma>;
+  const size_t smem = tck_smem_bytes<NR>(p);
+  auto kern = p.positions != nullptr ? verify_attn_tck_kernel<NR, kTma, true> : verify_attn_tck_kernel<NR, kTma, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // cooperative: every CTA is resident, so the wait for a segment's parts ends

@@ -46,6 +46,7 @@
 #include "va_kernels.h"
 #include "va_merge.cuh"
 #include "va_pipeline.cuh"
+#include "va_rope_fused.cuh"
 #include "va_tcgen05.cuh"
 
 namespace va {
@@ -63,7 +64,9 @@ struct TpSmem {
   static constexpr int kNumBars = 4 * kTpSlots + 3 * 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
   static constexpr int kLoFlagOff = kMiscOff + 16;          // int [2]: P residual written, per M-tile
-  static constexpr int kTstartOff = kLoFlagOff + 16;
+  // then the rotary table of the segment (rope_table_bytes, 0 without
+  // positions) and the tile starts of the work plan
+  static constexpr int kRopeOff = kLoFlagOff + 16;
   static constexpr int kThreads = 10 * 32;
   static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && Geo::kTileBytes % 1024 == 0, "swizzle atoms");
 };
@@ -158,6 +161,7 @@ __device__ __forceinline__ void tp_produce(const AttnParams &p, const CUtensorMa
   }
 }
 
+template <bool kRope>
 __global__ void __launch_bounds__(TpSmem::kThreads, 1)
     verify_attn_tcp_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv) {
@@ -184,7 +188,8 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
   volatile int *merge_ok = abort_flag + 1;
   volatile int *lo_flag = reinterpret_cast<volatile int *>(smem + SM::kLoFlagOff);
-  int *tstart = reinterpret_cast<int *>(smem + SM::kTstartOff);
+  float2 *rope_tab = reinterpret_cast<float2 *>(smem + SM::kRopeOff);
+  int *tstart = reinterpret_cast<int *>(smem + SM::kRopeOff + (kRope ? rope_table_bytes(p) : 0));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -248,6 +253,16 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
     const uint64_t dK0 = umma_sdesc(smem_u32(sK), 16, 1024);
     const uint64_t dV0 = umma_sdesc(smem_u32(sV), TK * 128, 1024);
     constexpr uint64_t kSlotStep = (uint64_t)(Geo::kTileBytes >> 4);
+    // the draft keys of tile lt of segment g, rotated in place before any S MMA reads them
+    auto rotate_draft = [&](int sl, const Seg &g, int lt) {
+      if (kRope && ok && lt * TK + TK > g.n_prefix) {
+        const int r0 = max(0, g.n_prefix - lt * TK), r1 = min(TK, g.nkeys - lt * TK);
+        rope_rotate_tile_rows<__nv_bfloat16, D, TK>(sK + sl * Geo::kTileBytes, r0, r1, lt * TK + r0 - g.n_prefix,
+                                                    rope_tab, lane, 32);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+    };
     auto issue_s = [&](int i, int sl) {  // S_i = Q_i K^T into TMEM 256 + 128 i
       if (!ok || lane != 0) return;
       tc_fence_after();
@@ -291,6 +306,7 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
       const int lt1 = min(tstart[s + 1], t1) - tstart[s];
       named_bar_sync(kBarQ, kSoft + 32);  // Q of this segment is in shared memory
       wait_ok(kfull + it % NSL, (uint32_t)(it / NSL) & 1u);
+      rotate_draft(it % NSL, g, lt0);
       issue_s(0, it % NSL);
       issue_s(1, it % NSL);
       commit(kempty + it % NSL);  // the K slot is free once both S MMAs have read it
@@ -321,7 +337,10 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
           if (i == 1) commit(vempty + sl);
           if (more) {
             wait_ok(o_done + i, jph);  // PV_i(t) has read P_i: S_i(t+1) may overwrite it
-            if (i == 0) wait_ok(kfull + (it + 1) % NSL, (uint32_t)((it + 1) / NSL) & 1u);
+            if (i == 0) {
+              wait_ok(kfull + (it + 1) % NSL, (uint32_t)((it + 1) / NSL) & 1u);
+              rotate_draft((it + 1) % NSL, g, lt + 1);
+            }
             issue_s(i, (it + 1) % NSL);
             if (i == 1) commit(kempty + (it + 1) % NSL);
           }
@@ -346,6 +365,7 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
   const uint32_t tO = tmem + lane_bits + 128 * mi;
   const uint32_t tS = tmem + lane_bits + 256 + 128 * mi;
   int jt = 0;
+  int rope_b = -1;  // sequence whose rotary table is in shared memory
   // split segments this CTA holds a part of (at most its first and its last)
   int n_split = 0, ms[2] = {0, 0}, mslot[2] = {0, 0}, mnp[2] = {0, 0}, mpart[2] = {0, 0};
   for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
@@ -359,7 +379,34 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
     // ---- Q of this segment into shared memory (both warpgroups; every S MMA
     // of the previous segment has completed once both have passed here) ----
     named_bar_sync(kBarSoft, kSoft);
-    {
+    if constexpr (kRope) {
+      // rotary table of this sequence's draft tokens (kept while the CTA stays
+      // on the sequence), then q rotated on its way in
+      if (g.b != rope_b) {
+        rope_build_table(p, g.b, rope_tab, tid, kSoft);
+        named_bar_sync(kBarSoft, kSoft);
+        rope_b = g.b;
+      }
+      const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+      for (int e = tid; e < 2 * 128 * 8; e += kSoft) {
+        const int m = e >> 10;
+        const int row = (e >> 3) & 127;
+        const int ch = e & 7;
+        const int rr = g.rb * p.rows_pad + m * 128 + row;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (rr < p.R) {
+          const int t = rr / group;
+          const int hq = g.hkv * group + rr % group;
+          const uint4 *src = reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D);
+          lo = __ldg(src + ch);
+          hi = __ldg(src + ch + 8);
+          rope_rotate8_bf16(lo, hi, rope_tab + t * (D / 2) + ch * 8);
+        }
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + tp_swz(row, ch)) = lo;
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + tp_swz(row, ch + 8)) = hi;
+      }
+      fence_proxy_async_smem();
+    } else {
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
       for (int e = tid; e < 2 * 128 * 16; e += kSoft) {
         const int m = e >> 11;
@@ -606,13 +653,13 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 size_t attn_tcp_smem_required(const AttnParams &p) {
-  return 1024 + (size_t)TpSmem::kTstartOff + (size_t)(p.S + 1) * 4;
+  return 1024 + (size_t)TpSmem::kRopeOff + (size_t)rope_table_bytes(p) + (size_t)(p.S + 1) * 4;
 }
 
 cudaError_t launch_attention_tcp(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
                                  cudaStream_t stream) {
   const size_t smem = attn_tcp_smem_required(p);
-  auto kern = verify_attn_tcp_kernel;
+  auto kern = p.positions != nullptr ? verify_attn_tcp_kernel<true> : verify_attn_tcp_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // cooperative: every CTA is resident, so the wait for a segment's parts ends

@@ -39,6 +39,10 @@ struct AttnParams {
   const int32_t *parent;
   const uint32_t *mask;
   int mask_words;
+  // rotary embedding on the fly: positions [B][T] (NULL: q and the draft keys
+  // are used as stored) and base^(-2i/D) split into fp32 high and low parts
+  const int32_t *positions;
+  float rope_fhi[64], rope_flo[64];
   // outputs
   void *out;
   int out_align16;  // out is 16-byte aligned (bulk copies allowed)

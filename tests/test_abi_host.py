@@ -40,15 +40,15 @@ FAKE = 1 << 20  # a non-NULL address validation never dereferences
 
 
 def _shape(**kw):
-    d = dict(B=1, T=8, Hq=32, Hkv=8, D=128, dtype=0, scale=0.088)
+    d = dict(B=1, T=8, Hq=32, Hkv=8, D=128, dtype=0, scale=0.088, rope_base=0.0)
     d.update(kw)
-    return api.VaShape(d["B"], d["T"], d["Hq"], d["Hkv"], d["D"], d["dtype"], d["scale"])
+    return api.VaShape(d["B"], d["T"], d["Hq"], d["Hkv"], d["D"], d["dtype"], d["scale"], d["rope_base"])
 
 
-def _dense(shape, parent=None, mask=None, ws=FAKE, q=FAKE, max_len=100):
+def _dense(shape, parent=None, mask=None, ws=FAKE, q=FAKE, max_len=100, positions=None):
     L = api.lib()
     return L.verify_attn_dense(ctypes.byref(shape) if shape is not None else None, q, FAKE, FAKE, max_len, FAKE,
-                               parent, mask, None, FAKE, FAKE, ws, 1 << 30, None)
+                               parent, mask, positions, FAKE, FAKE, ws, 1 << 30, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -64,6 +64,15 @@ def _dense(shape, parent=None, mask=None, ws=FAKE, q=FAKE, max_len=100):
 def test_bad_shapes_rejected_on_host(kw, code):
     assert _dense(_shape(**kw)) == code
     assert api.lib().verify_attn_last_error()
+
+
+def test_rotation_on_the_fly_needs_a_base():
+    """positions given: the shape must carry the model's RoPE base (checked
+    before anything is enqueued)."""
+    assert _dense(_shape(), positions=FAKE) == api.VA_ERR_INVALID_ARG
+    assert "rope_base" in api.lib().verify_attn_last_error().decode()
+    assert _dense(_shape(rope_base=float("nan")), positions=FAKE) == api.VA_ERR_INVALID_ARG
+    assert _dense(_shape(rope_base=-1.0), positions=FAKE) == api.VA_ERR_INVALID_ARG
 
 
 def test_bad_pointers_rejected_on_host():

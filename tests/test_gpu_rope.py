@@ -231,3 +231,134 @@ def test_rope_rows_not_16_byte_aligned():
     for b in range(B):
         rows = slice(int(L[b]), int(L[b]) + T)
         _close(gk[b, rows], want_k[b, rows], kh[b, rows], torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------
+# rotation inside the attention kernels (positions passed to verify_attn_*)
+# ----------------------------------------------------------------------------
+
+def _to_dtype(x64, dtype):
+    """The oracle's f64 rotation rounded once to the element type (what the
+    separate rotation pass stores and the fused kernels feed their MMAs)."""
+    return torch.from_numpy(np.ascontiguousarray(x64)).to(dtype)
+
+
+def _rotated_copy(w, pos, base):
+    """A copy of workload w whose q and draft key rows carry the oracle's
+    rotation at pos (rounded to w's element type)."""
+    import copy
+
+    r = copy.copy(w)
+    dt = w.q.dtype
+    if w.layout == "paged":
+        q64, k64 = oracle.rope_draft_paged(_host(w.q), _host(w.k_pages), w.page_table, w.page_size, w.seqlens, pos,
+                                           base)
+        r.k_pages = _to_dtype(k64, dt)
+    else:
+        q64, k64 = oracle.rope_draft_dense(_host(w.q), _host(w.k_cache), w.seqlens, pos, base)
+        r.k_cache = _to_dtype(k64, dt)
+    r.q = _to_dtype(q64, dt)
+    return r
+
+
+FUSED_CASES = {
+    # keys on TMEM lanes: 16 / 32 / 64 packed rows, TMA tiles and gathers
+    "tck16_dense": ("chain", dict(B=2, Hq=8, Hkv=2, T=4, L_lo=1500, L_hi=3000), "parent", None),
+    "tck32_dense": ("chain", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=5000), "parent", None),
+    "tck64_paged16": ("paged", dict(B=3, Hkv=2, Hq=8, L_lo=1500, L_hi=2500, page_size=16), "mask", None),
+    "tck64_paged4": ("paged", dict(B=3, Hkv=2, Hq=8, L_lo=1500, L_hi=2500, page_size=4), "mask", None),
+    "tck32_sparse": ("sparse", dict(B=2, Hkv=2, Hq=8, T=8, L_lo=3000, L_hi=5000, budget=600, m_draft=200,
+                                    window=64), "parent", None),
+    # rows on TMEM lanes: one and two M-tiles, 64-key kernel and the two-M-tile kernel
+    "tc1_dense": ("tree", dict(B=2, Hkv=2, Hq=8, T=24, L=2600, depth=4), "parent", None),
+    "tc2_dense": ("tree", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=3000), "parent", None),
+    "tcp_dense": ("tree", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=3000), "parent", ("VA_MANY_ROWS_KERNEL", "tcp")),
+    "tc1_paged16": ("paged", dict(B=2, Hkv=2, Hq=8, T=32, L_lo=1500, L_hi=2000, page_size=16, tree="depth", depth=5),
+                    "parent", None),
+    "tc2_sparse": ("sparse", dict(B=1, Hkv=2, Hq=8, T=40, L_lo=3000, L_hi=4000, budget=700, m_draft=200, window=64,
+                                  tree="depth", depth=5), "parent", None),
+    # mma.sync (bf16 d64, and d128 by route) and the fp32 SIMT path
+    "mma_d64": ("chain", dict(B=2, Hq=32, Hkv=8, T=5, D=64, L_lo=1500, L_hi=3000), "parent", None),
+    "mma_d128": ("chain", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=3000), "parent", ("VA_SMALL_ROWS_KERNEL", "mma")),
+    "fp32_tiny": ("tiny", dict(L=3000), "parent", None),
+}
+
+
+@pytest.mark.parametrize("kind", ["tree", "anchor", "large"])
+@pytest.mark.parametrize("case", list(FUSED_CASES))
+def test_rotation_inside_attention_matches_oracle(case, kind, monkeypatch):
+    """One fused call on unrotated q and cache against the rotation oracle
+    followed by the attention oracle, strict bars (prefixes of 1500 tokens or
+    more keep |out| well below 0.5, where the bf16 rounding of the output
+    itself stays under 1e-3); q and the cache are left untouched by the call."""
+    name, over, mode, env = FUSED_CASES[case]
+    if env is not None:
+        monkeypatch.setenv(*env)
+    w = W.make_workload(name, seed=len(case) * 31 + len(kind), **over)
+    rng = np.random.default_rng(len(case) + 7 * len(kind))
+    parent = w.parent if w.parent is not None else np.tile(np.arange(-1, w.T - 1), (w.B, 1))
+    pos = _positions(kind, w.seqlens, w.T, parent, rng)
+    base = 500000.0 if kind == "large" else 10000.0
+    ref_w = _rotated_copy(w, pos, base)
+    kw = {}
+    if w.layout == "sparse":
+        ref = oracle.verify(ref_w)
+        kw = dict(indices=dev_i32(ref["indices"]), n_indices=dev_i32(ref["n_indices"]))
+    else:
+        ref = oracle.verify(ref_w)
+    q = w.q.cuda()
+    seqlens, dpos = dev_i32(w.seqlens), dev_i32(pos)
+    drafts = dict(tree_parent=dev_i32(w.parent)) if mode == "parent" else dict(tree_mask=torch.from_numpy(
+        np.ascontiguousarray(w.mask_words).view(np.int32)).cuda())
+    if w.layout == "paged":
+        k, v = w.k_pages.cuda(), w.v_pages.cuda()
+        out, lse = va.verify_attn_paged(q, k, v, dev_i32(w.page_table), seqlens, positions=dpos, rope_base=base,
+                                        **drafts)
+    elif w.layout == "sparse":
+        k, v = w.k_cache.cuda(), w.v_cache.cuda()
+        out, lse = va.verify_attn_sparse(q, k, v, seqlens, kw["indices"], kw["n_indices"], positions=dpos,
+                                         rope_base=base, **drafts)
+    else:
+        k, v = w.k_cache.cuda(), w.v_cache.cuda()
+        out, lse = va.verify_attn_dense(q, k, v, seqlens, positions=dpos, rope_base=base, **drafts)
+    torch.cuda.synchronize()
+    if w.dtype == "fp32":
+        compare(out, lse, ref, tol_out=1e-4, tol_lse=1e-4, strict=True)
+    else:
+        compare(out, lse, ref, strict=True)
+    # nothing the caller passed in is written
+    assert torch.equal(q.cpu(), w.q)
+    assert torch.equal(k.cpu(), w.k_pages if w.layout == "paged" else w.k_cache)
+
+
+def test_rotation_inside_attention_noalloc_and_equal_to_the_pass():
+    """The fused rotation through the allocation-free entry point, and against
+    the separate pass followed by an unrotated call: the same bf16 inputs reach
+    the MMAs in both, so the results agree to the last bits but for the
+    rounding of the rotation itself (fp32 in the kernels, fp64 in the pass)."""
+    w = W.make_workload("chain", seed=301, L=4000)
+    pos = (w.seqlens[:, None] + np.arange(w.T)[None]).astype(np.int32)
+    q, k, v = w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda()
+    seqlens, dpos, par = dev_i32(w.seqlens), dev_i32(pos), dev_i32(w.parent)
+    fused, lse_f = va.api.verify_attn_dense_noalloc(q, k, v, seqlens, tree_parent=par, positions=dpos,
+                                                    rope_base=10000.0)
+    q2, k2 = q.clone(), k.clone()
+    va.verify_rope_draft_dense(q2, k2, seqlens, dpos, 10000.0)
+    sep, lse_s = va.verify_attn_dense(q2, k2, v, seqlens, tree_parent=par)
+    torch.cuda.synchronize()
+    assert float((fused.float() - sep.float()).abs().max()) <= 2e-3
+    assert float((lse_f - lse_s).abs().max()) <= 1e-3
+    compare(fused, lse_f, oracle.verify(_rotated_copy(w, pos, 10000.0)), strict=True)
+
+
+def test_rotation_inside_attention_position_out_of_range_is_reported():
+    w = W.make_workload("chain", seed=302, L=500)
+    pos = (w.seqlens[:, None] + np.arange(w.T)[None]).astype(np.int32)
+    pos[0, 3] = 1 << 25
+    shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0, rope_base=10000.0)
+    ws = va.Workspace.for_shape(shape)
+    va.verify_attn_dense(w.q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), dev_i32(w.seqlens),
+                         tree_parent=dev_i32(w.parent), positions=dev_i32(pos), rope_base=10000.0, workspace=ws)
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(ws)
+    assert ei.value.status == va.api.VA_ERR_DEVICE_BOUNDS
