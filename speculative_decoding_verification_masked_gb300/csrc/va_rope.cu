@@ -7,7 +7,8 @@
 // of the cache, at the angle positions[b][t] * base^(-2i/D) for the pair
 // (i, i + D/2) (rotate-half layout).  The inverse frequencies base^(-2i/D)
 // come from the host in fp64; each angle is formed and reduced modulo 2 pi in
-// fp64 (five fp64 operations), so that ids far beyond 2^24 radians of phase
+// fp64 (five fp64 operations, a Cody-Waite reduction with 2 pi in two parts),
+// so that ids far beyond 2^24 radians of phase
 // keep their precision; sine and cosine of the reduced angle are taken in fp32 and
 // shared by all rows of the token through shared memory.  Rows are rotated
 // in fp32 and written back in their own element type (bf16: round to nearest
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(128) rope_draft_kernel(const RopeParams p) {
   const bool kv_ok = L >= 0 && L <= p.len_cap - p.T;
   if (!kv_ok && t == 0 && tid == 0) record_status(p.status, VA_ERR_DEVICE_BOUNDS);
   for (int i = tid; i < half; i += blockDim.x) {
-    // a_i = pos * base^(-2i/D), reduced to [-pi, pi] in fp64 (2 pi in two parts)
+    // a_i = pos * base^(-2i/D), reduced to [-pi, pi] in fp64 by the Cody-Waite
+    // method: k = rint(a / 2pi), r = (a - k C1) - k C2 with 2 pi split into its
+    // fp64 rounding C1 and the fp64 rounding C2 of the remainder 2pi - C1
+    // (values of 2 pi and 1 / 2pi to 17 significant digits)
     const double a = (double)pos * p.inv_freq[i];
     const double kq = rint(a * 0.15915494309189535);
     const double r = fma(-kq, 2.4492935982947064e-16, fma(-kq, 6.283185307179586, a));
