@@ -90,7 +90,8 @@ typedef enum {
   VA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
   VA_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   VA_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out */
-  VA_ERR_DEVICE_BOUNDS = 6  /* device: seqlen / page / index out of range */
+  VA_ERR_DEVICE_BOUNDS = 6, /* device: seqlen / page / index out of range */
+  VA_ERR_DEVICE_INVALID = 7 /* device, validation mode: a verify set that is not strictly increasing */
 } va_status;
 
 typedef enum { VA_DTYPE_BF16 = 0, VA_DTYPE_FP32 = 2 } va_dtype;
@@ -189,8 +190,14 @@ va_status verify_attn_paged(const va_shape *shape, const void *q, const void *k_
  * to the cache rows listed in the verify set of its (sequence, kv-head); the
  * cache itself is not compacted.  indices [B][Hkv][max_indices] int32 with
  * n_indices [B][Hkv] valid entries each, every entry in [0, L_b) (device
- * checked); order does not matter for the result.  The draft block is always
- * read from the dense slots L_b..L_b+T-1 under the draft mask.
+ * checked); order does not matter for the result, but a verify set is a set:
+ * an index listed twice is attended twice.  The draft block is always read
+ * from the dense slots L_b..L_b+T-1 under the draft mask.
+ * Validation mode: with the environment variable VA_DEBUG_VALIDATE=1 the call
+ * first checks every row on the device -- n_indices in [0, max_indices] and
+ * its entries strictly increasing inside [0, L_b), the form verify_build_index
+ * writes -- and records VA_ERR_DEVICE_INVALID for a row with an entry out of
+ * order or listed twice (VA_ERR_DEVICE_BOUNDS for one out of range).
  */
 va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k_cache,
                              const void *v_cache, int max_cache_len, const int32_t *seqlens,

@@ -18,10 +18,10 @@ import torch
 from . import build as _build
 
 VA_OK, VA_ERR_INVALID_ARG, VA_ERR_UNSUPPORTED, VA_ERR_WORKSPACE, VA_ERR_CUDA, VA_ERR_TIMEOUT, \
-    VA_ERR_DEVICE_BOUNDS = range(7)
+    VA_ERR_DEVICE_BOUNDS, VA_ERR_DEVICE_INVALID = range(8)
 VA_DTYPE_BF16, VA_DTYPE_FP32 = 0, 2
 STATUS_NAMES = {0: "VA_OK", 1: "VA_ERR_INVALID_ARG", 2: "VA_ERR_UNSUPPORTED", 3: "VA_ERR_WORKSPACE",
-                4: "VA_ERR_CUDA", 5: "VA_ERR_TIMEOUT", 6: "VA_ERR_DEVICE_BOUNDS"}
+                4: "VA_ERR_CUDA", 5: "VA_ERR_TIMEOUT", 6: "VA_ERR_DEVICE_BOUNDS", 7: "VA_ERR_DEVICE_INVALID"}
 
 
 class VerifyAttnError(RuntimeError):

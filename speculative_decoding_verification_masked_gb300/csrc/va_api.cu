@@ -66,6 +66,13 @@ std::atomic<int> g_test_drop_part{-1};
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// VA_DEBUG_VALIDATE=1: check inputs on the device that the fast path trusts
+// (read at every call, so a test may switch it per call)
+bool debug_validate() {
+  const char *e = getenv("VA_DEBUG_VALIDATE");
+  return e != nullptr && strcmp(e, "1") == 0;
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -457,6 +464,13 @@ va_status verify_attn_sparse(const va_shape *shape, const void *q, const void *k
   if (max_cache_len < shape->T)
     return fail(VA_ERR_INVALID_ARG, "max_cache_len=%d is smaller than T=%d", max_cache_len, shape->T);
   if (max_indices < 0) return fail(VA_ERR_INVALID_ARG, "max_indices must be >= 0");
+  if (debug_validate()) {
+    // validation mode: the verify sets are checked on the device first
+    cudaError_t e = va::launch_validate_index(shape->B, shape->Hkv, seqlens, indices, n_indices, max_indices,
+                                              max_cache_len, shape->T, static_cast<int *>(workspace),
+                                              (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "validation launch");
+  }
   return run_attention(c, VA_LAYOUT_SPARSE, k_cache, v_cache, max_cache_len, 0, 1, nullptr, 0, indices, n_indices,
                        max_indices, (cudaStream_t)stream);
 }
@@ -712,6 +726,9 @@ va_status verify_attn_check_status(void *workspace, va_stream stream) {
         return fail(VA_ERR_TIMEOUT, "a bounded device wait ran out");
       case VA_ERR_DEVICE_BOUNDS:
         return fail(VA_ERR_DEVICE_BOUNDS, "device saw an out-of-range seqlen, page, index or parent");
+      case VA_ERR_DEVICE_INVALID:
+        return fail(VA_ERR_DEVICE_INVALID, "validation: a verify set is not strictly increasing (out of order or "
+                                           "an index listed twice)");
       default:
         return fail((va_status)status, "device status %d", status);
     }

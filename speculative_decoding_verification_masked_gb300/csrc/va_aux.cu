@@ -424,6 +424,37 @@ cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const flo
 }
 
 // ---------------------------------------------------------------------------
+// validation mode of the sparse call: every verify set strictly increasing
+// inside [0, L_b) (a set, in the form the index builder writes)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) validate_index_kernel(int Hkv, const int32_t *seqlens, const int32_t *indices,
+                                                            const int32_t *n_indices, int max_indices, int len_cap,
+                                                            int T, int *status) {
+  const int row = blockIdx.x;
+  const int b = row / Hkv;
+  const int L = min(max(__ldg(seqlens + b), 0), max(len_cap - T, 0));
+  const int n = __ldg(n_indices + row);
+  if (n < 0 || n > max_indices) {
+    if (threadIdx.x == 0) record_status(status, VA_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int32_t *idx = indices + (size_t)row * max_indices;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int v = __ldg(idx + j);
+    if (v < 0 || v >= L) record_status(status, VA_ERR_DEVICE_BOUNDS);
+    else if (j + 1 < n && __ldg(idx + j + 1) <= v) record_status(status, VA_ERR_DEVICE_INVALID);
+  }
+}
+
+cudaError_t launch_validate_index(int B, int Hkv, const int32_t *seqlens, const int32_t *indices,
+                                  const int32_t *n_indices, int max_indices, int len_cap, int T, int *status,
+                                  cudaStream_t stream) {
+  validate_index_kernel<<<B * Hkv, 256, 0, stream>>>(Hkv, seqlens, indices, n_indices, max_indices, len_cap, T,
+                                                     status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // bounded-wait self test: waits on an mbarrier nothing will ever complete;
 // the wait must give up after wait_ns and record VA_ERR_TIMEOUT.
 // ---------------------------------------------------------------------------

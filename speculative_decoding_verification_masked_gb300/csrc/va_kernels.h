@@ -79,5 +79,8 @@ cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const flo
                                const float *score_target, int score_stride, int n_sink, int window, int m_draft,
                                int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t wait_ns, cudaStream_t stream);
+cudaError_t launch_validate_index(int B, int Hkv, const int32_t *seqlens, const int32_t *indices,
+                                  const int32_t *n_indices, int max_indices, int len_cap, int T, int *status,
+                                  cudaStream_t stream);
 
 }  // namespace va

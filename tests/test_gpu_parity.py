@@ -266,6 +266,39 @@ def test_sparse_small_with_library_indices():
     compare(out, lse, ref)
 
 
+def test_debug_validation_of_verify_sets(monkeypatch):
+    """VA_DEBUG_VALIDATE=1: a verify set with an index listed twice, or out of
+    order, is reported on the device (the fast path would attend a duplicate
+    twice); the sets the builder writes pass.  The bad rows are made on the host."""
+    w = W.make_workload("sparse", seed=3, B=3, L_lo=200, L_hi=900, budget=256, window=32, n_sink=4, m_draft=60)
+    ref = oracle.verify(w)
+    monkeypatch.setenv("VA_DEBUG_VALIDATE", "1")
+    shape = va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0)
+
+    def call(idx):
+        ws = va.Workspace.for_shape(shape)
+        run_library(w, "parent", indices=dev_i32(idx), n_indices=dev_i32(ref["n_indices"]), workspace=ws)
+        return ws
+
+    out_ws = call(ref["indices"])
+    va.verify_attn_check_status(out_ws)  # the builder's sets are valid
+    dup = ref["indices"].copy()
+    dup[1, 0, 7] = dup[1, 0, 6]  # listed twice
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(call(dup))
+    assert ei.value.status == va.api.VA_ERR_DEVICE_INVALID
+    swapped = ref["indices"].copy()
+    swapped[2, 1, [10, 11]] = swapped[2, 1, [11, 10]]  # out of order
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(call(swapped))
+    assert ei.value.status == va.api.VA_ERR_DEVICE_INVALID
+    far = ref["indices"].copy()
+    far[0, 0, 5] = 10 ** 6  # past the sequence
+    with pytest.raises(va.VerifyAttnError) as ei:
+        va.verify_attn_check_status(call(far))
+    assert ei.value.status == va.api.VA_ERR_DEVICE_BOUNDS
+
+
 def test_sparse_full_index_equals_dense_on_gpu():
     w = W.make_workload("sparse", seed=4, B=2, L_lo=100, L_hi=300, budget=512, window=8, n_sink=2, m_draft=3)
     Lmax = int(w.seqlens.max())
