@@ -601,18 +601,29 @@ def rope_oracle_sample(B=4):
 
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture of it
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the sources
-# that kernel is built from hash to those captured.
-PROFILED_TRAFFIC = {}
-KERNEL_SOURCES = ["va_attn_tck.cu", "va_pipeline.cuh", "va_common.cuh", "va_tcgen05.cuh", "va_kernels.h"]
+# (dram__bytes_read.sum + dram__bytes_write.sum, the --set full capture of
+# `bench.py --profile <config>`), valid only while the sources that kernel is
+# built from hash to those captured.
+_HEADERS = ['va_common.cuh', 'va_pipeline.cuh', 'va_tcgen05.cuh', 'va_kernels.h', 'va_rope_fused.cuh', 'va_merge.cuh']
+KERNEL_SOURCES = {"tc": ["va_attn_tc.cu"] + _HEADERS, "tck": ["va_attn_tck.cu"] + _HEADERS}
+PROFILED_TRAFFIC = {
+    "tree": {"sources": "tc", "sha256": "70c3e5370bd4bfe32946a381be3be85a5f4c2aded4ee0a821a09271d87644a4a",
+             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541208832},
+    "chain": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
+              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137794816},
+    "sparse": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
+               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141123584},
+    "paged": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
+              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470923264},
+}
 
 
-def kernel_sources_sha256():
+def kernel_sources_sha256(which):
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_masked_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[which]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -620,7 +631,7 @@ def kernel_sources_sha256():
 
 def profiled_traffic(config):
     rec = PROFILED_TRAFFIC.get(config)
-    if rec is None or rec["sha256"] != kernel_sources_sha256():
+    if rec is None or rec["sha256"] != kernel_sources_sha256(rec["sources"]):
         return None
     return rec["bytes"]
 
