@@ -36,8 +36,9 @@
  *   tree_parent  [B][T] int32         -1 for a root, else 0 <= parent[i] < i
  *   tree_mask    [B][T][W] uint32     W = ceil(T/32); bit j%32 of word j/32 of
  *                                     row i set = draft token i sees draft token j
- *   positions    [B][T] int32         position id of draft token t (read only by
- *                                     verify_rope_draft_*; see there)
+ *   positions    [B][T] int32         position id of draft token t (NULL = q and
+ *                                     the draft keys already rotated; see
+ *                                     "Rotary embedding" below)
  * Draft keys.  The T draft tokens' keys and values are already in the cache at
  *   logical slots L_b .. L_b+T-1 (append, then verify; rejected entries are
  *   dropped afterwards).
