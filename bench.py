@@ -648,7 +648,7 @@ def attention_path(w):
           and (w.layout == "dense" or (w.layout == "paged" and w.page_size >= 8))):
         kernel, launches = "verify_attn_tcp_kernel (two M-tiles of rows on TMEM lanes, LSE merge inside)", 1
     elif w.dtype == "bf16" and w.D == 128:
-        kernel, launches = "verify_attn_tc_kernel (rows on TMEM lanes) + split-segment merge kernel", 2
+        kernel, launches = "verify_attn_tc_kernel (rows on TMEM lanes, LSE merge inside)", 1
     else:
         kernel, launches = "verify_attn_kernel (mma.sync / fp32 SIMT) + split-segment merge kernel", 2
     if w.layout == "sparse":

@@ -800,7 +800,7 @@ cudaError_t launch_attention(const AttnParams &p, const CUtensorMap &tmk, const 
                              cudaStream_t stream) {
   cudaError_t e;
   if (p.use_tc == 1) {
-    e = launch_attention_tc(p, tmk, tmv, grid, stream);
+    return launch_attention_tc(p, tmk, tmv, grid, stream);  // merges its split segments itself
   } else if (p.use_tc == 2) {
     return launch_attention_tck(p, tmk, tmv, grid, stream);  // merges its split segments itself
   } else if (p.use_tc == 3) {

@@ -6,7 +6,8 @@
 // 64-key tiles), but every K/V tile read from HBM now feeds up to 256 query
 // rows through UMMA instead of warp-level mma.sync.
 //
-// Roles (11 warps when the segment has two 128-row M-tiles):
+// Roles (12 warps when the segment has two 128-row M-tiles; one CTA per SM,
+// cooperative launch):
 //   warps 0-3 / 4-7  softmax warpgroup of M-tile 0 / 1: thread = one query row
 //                    = one TMEM lane.  Reads S from TMEM, applies the draft
 //                    bitmask, runs the online softmax, writes P (bf16) back
@@ -34,6 +35,9 @@
 //                    are not ordered against each other); with S and PV on
 //                    separate warps neither waits behind the other's issue.
 // TMEM (512 columns): O_i at 128*i, S/P buffers at 256 + 64*(2*i + b).
+// A segment cut over several CTAs leaves one normalised part per CTA; after
+// its last tile every CTA of the segment waits (bounded) for all parts and
+// merges an equal share of the rows by their log-sum-exp.
 // Every wait is bounded; on timeout the CTA records VA_ERR_TIMEOUT, keeps the
 // barrier sequence of all roles intact, drains and frees TMEM.
 #include <cuda.h>
@@ -41,6 +45,7 @@
 
 #include "va_common.cuh"
 #include "va_kernels.h"
+#include "va_merge.cuh"
 #include "va_pipeline.cuh"
 #include "va_rope_fused.cuh"
 #include "va_tcgen05.cuh"
@@ -60,7 +65,7 @@ struct TcSmem {
   static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
   // barriers: full[NS], empty[NS], s_full[2][2], p_full[2][2], o_done[2][2], drain
   static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
   static constexpr int kLoFlagOff = kMiscOff + 16;          // int [2][2]: P residual written, per M-tile and buffer
   // then the rotary table of the segment (rope_table_bytes, 0 without
   // positions) and the tile starts of the work plan
@@ -100,6 +105,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   uint64_t *drain = bars + 2 * NS + 12;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kMiscOff + 4);
+  volatile int *merge_ok = abort_flag + 1;
   float2 *rope_tab = reinterpret_cast<float2 *>(smem + SM::kRopeOff);
   int *tstart = reinterpret_cast<int *>(smem + SM::kRopeOff + (kRope ? rope_table_bytes(p) : 0));
   volatile int *lo_flag = reinterpret_cast<volatile int *>(smem + SM::kLoFlagOff);
@@ -283,17 +289,15 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
   };
   int jt = 0;
   int rope_b = -1;  // sequence whose rotary table is in shared memory
+  // split segments this CTA holds a part of (at most its first and its last)
+  int n_split = 0, ms[2] = {0, 0}, mslot[2] = {0, 0}, mnp[2] = {0, 0}, mpart[2] = {0, 0};
   for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
     const Seg g = seg_info(p, s, false);
     const int lt0 = max(tstart[s], t0) - tstart[s];
     const int lt1 = min(tstart[s + 1], t1) - tstart[s];
     const int first_cta = owner_cta(tstart[s], cr.total, cr.G);
     const int n_parts = owner_cta(tstart[s + 1] - 1, cr.total, cr.G) - first_cta + 1;
-    if (lt0 == 0 && tid == 0) {
-      p.meta[s] = make_int2(s + first_cta, n_parts);
-      if (n_parts > 1)  // one entry per split segment
-        p.split_list[atomicAdd(p.split_count, 1)] = make_int4(s, s + first_cta, n_parts, 0);
-    }
+    if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
 
     // ---- Q of this segment into shared memory (both warpgroups) ----
     named_bar_sync(kBarSoft, kSoftThreads);  // previous segment's MMAs have all completed
@@ -362,16 +366,15 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       wait_ok(s_full + 2 * mi + b, (uint32_t)(jt >> 1) & 1u);
       tc_fence_after();
       float sv[64];
-      {
-        uint32_t u[32];
+      {  // both halves in flight before the one wait
+        uint32_t u[32], w[32];
         tmem_ld32(tS, u);
+        tmem_ld32(tS + 32, w);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(u[j]);
-        tmem_ld32(tS + 32, u);
-        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(u[j]);
+        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(w[j]);
       }
       const int k0 = lt * kTK;
       const bool masked = k0 + kTK > g.n_prefix;
@@ -502,6 +505,41 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       else
         p.lse_part[(size_t)(s + c) * p.rows_pad + mi * 128 + r] = lse_nat;
     }
+    if (n_parts > 1) {
+      // publish the part (always, also after a failed wait, so the counters
+      // return to zero): the barrier orders every warpgroup's row and lse
+      // stores before thread 0's release increment, which is cumulative
+      named_bar_sync(kBarSoft, kSoftThreads);
+      if (tid == 0 && c != p.test_drop_part)
+        red_release_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * n_parts - 1u);
+      if (n_split < 2) {
+        ms[n_split] = s;
+        mslot[n_split] = s + first_cta;
+        mnp[n_split] = n_parts;
+        mpart[n_split] = c - first_cta;
+        ++n_split;
+      }
+    }
+  }
+
+  // ---- merge of the split segments (LongSpec 2.C): once every part of a
+  // segment has arrived, each of its CTAs merges an equal share of its rows ----
+  for (int k = 0; k < n_split; ++k) {
+    const int s = ms[k], np = mnp[k];
+    if (tid == 0) *merge_ok = wait_parts_arrived(p, s, np) ? 1 : 0;
+    named_bar_sync(kBarSoft, kSoftThreads);  // thread 0's acquire, then the barrier, orders the reads below
+    if (*merge_ok) {
+      const int rb = s % p.NRB, hkv = (s / p.NRB) % p.Hkv, b = s / (p.NRB * p.Hkv);
+      const int nrows = min(p.rows_pad, p.R - rb * p.rows_pad);
+      const int r0 = mpart[k] * nrows / np, r1 = (mpart[k] + 1) * nrows / np;
+      if (np <= 4)
+        merge_rows_warp<8, 4>(p, b, hkv, rb * p.rows_pad, mslot[k], np, r0, r1, warp, 4 * NMT, lane);
+      else
+        merge_rows_warp<32, 24>(p, b, hkv, rb * p.rows_pad, mslot[k], np, r0, r1, warp, 4 * NMT, lane);
+    }
+    named_bar_sync(kBarSoft, kSoftThreads);
+    // leave: np arrivals and np departures wrap the counter back to zero
+    if (tid == 0) red_relaxed_inc_gpu(reinterpret_cast<unsigned *>(&p.merge_cnt[s].x), 2u * np - 1u);
   }
   tc_fence_before();
   named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);
@@ -528,8 +566,18 @@ static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, cons
   auto kern = p.positions != nullptr ? verify_attn_tc_kernel<NMT, kTma, true> : verify_attn_tc_kernel<NMT, kTma, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, TcSmem<NMT>::kThreads, smem, stream>>>(p, tmk, tmv);
-  return cudaGetLastError();
+  // cooperative: every CTA is resident, so the wait for a segment's parts ends
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(TcSmem<NMT>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
 }
 
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,

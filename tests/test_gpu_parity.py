@@ -482,10 +482,14 @@ def test_timeout_then_recovery():
         compare(out, lse, oracle.verify(w), strict=True)
 
 
-def test_timeout_then_recovery_many_rows(monkeypatch):
-    """The same injected timeout in the two-M-tile kernel (tree workload shape,
+@pytest.mark.parametrize("kernel", ["tc", "tcp"])
+def test_timeout_then_recovery_many_rows(kernel, monkeypatch):
+    """The same injected timeout in the many-row kernels (tree workload shape,
     two kv-heads): every segment is cut over many CTAs."""
-    monkeypatch.setenv("VA_MANY_ROWS_KERNEL", "tcp")
+    if kernel == "tcp":
+        monkeypatch.setenv("VA_MANY_ROWS_KERNEL", "tcp")
+    else:
+        monkeypatch.delenv("VA_MANY_ROWS_KERNEL", raising=False)
     L = va.api.lib()
     w = W.make_workload("tree", seed=206, Hkv=2, Hq=8, L=20000)
     ws = va.Workspace.for_shape(va.make_shape(w.B, w.T, w.Hq, w.Hkv, w.D, 0))
