@@ -388,14 +388,16 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
         }
       }
       float mx;
-      {  // pairwise max: short dependency chains
+      {  // three-input maxima: 32 instructions, short dependency chains
+        float m22[22];
+#pragma unroll
+        for (int q = 0; q < 21; ++q) m22[q] = max3f(sv[3 * q], sv[3 * q + 1], sv[3 * q + 2]);
+        m22[21] = sv[63];
         float m8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          m8[q] = fmaxf(fmaxf(fmaxf(sv[8 * q], sv[8 * q + 1]), fmaxf(sv[8 * q + 2], sv[8 * q + 3])),
-                        fmaxf(fmaxf(sv[8 * q + 4], sv[8 * q + 5]), fmaxf(sv[8 * q + 6], sv[8 * q + 7])));
-        }
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int q = 0; q < 7; ++q) m8[q] = max3f(m22[3 * q], m22[3 * q + 1], m22[3 * q + 2]);
+        m8[7] = m22[21];
+        mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       }
       const float m_new = fmaxf(m_used, mx);
       // move the reference max only when it grew by more than 2^8 (exact either
@@ -420,15 +422,18 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       if (!masked) lo = bar_red_or(kBarVote + mi, 128, ex2_approx(fmaf(mx, cl2, -mu)) * 15.f > l);
       if (r == 0) lo_flag[2 * mi + b] = lo ? 1 : 0;
       uint32_t ph[32];
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short add chains
+      // packed pairs: the scaled argument and the running sums take one
+      // instruction per two scores
+      const float2 cl2v = make_float2(cl2, cl2), nmu = make_float2(-mu, -mu);
+      float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       if (lo) {
         // P as bf16 hi + lo parts (a second set of MMAs adds the lo parts)
         uint32_t pl[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float a = ex2_approx(fmaf(sv[2 * j], cl2, -mu));
-          const float bq = ex2_approx(fmaf(sv[2 * j + 1], cl2, -mu));
-          ls4[j & 3] += a + bq;
+          const float2 x = fma2(make_float2(sv[2 * j], sv[2 * j + 1]), cl2v, nmu);
+          const float a = ex2_approx(x.x), bq = ex2_approx(x.y);
+          ls2[j & 1] = add2(ls2[j & 1], make_float2(a, bq));
           split_bf16x2(a, bq, ph[j], pl[j]);
         }
         tmem_st32(tS, ph);
@@ -436,14 +441,14 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float a = ex2_approx(fmaf(sv[2 * j], cl2, -mu));
-          const float bq = ex2_approx(fmaf(sv[2 * j + 1], cl2, -mu));
-          ls4[j & 3] += a + bq;
+          const float2 x = fma2(make_float2(sv[2 * j], sv[2 * j + 1]), cl2v, nmu);
+          const float a = ex2_approx(x.x), bq = ex2_approx(x.y);
+          ls2[j & 1] = add2(ls2[j & 1], make_float2(a, bq));
           ph[j] = pack_bf16(a, bq);
         }
         tmem_st32(tS, ph);
       }
-      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      const float ls = (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
       l += ls;
       if (rescale) {
         // O relative to the new reference before PV(jt) adds to it; O holds

@@ -586,12 +586,15 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
           for (int q = 0; q < 4; ++q) {
             const int r = 8 * cc + 2 * q;
             // a row that has seen no key yet has mu = -inf and only -inf scores: P = 0
-            const float a = ex2_approx(fmaf(x[r], cl2, mu[r] == -INFINITY ? 0.f : -mu[r]));
-            const float bq = ex2_approx(fmaf(x[r + 1], cl2, mu[r + 1] == -INFINITY ? 0.f : -mu[r + 1]));
+            const float2 e = fma2(make_float2(x[r], x[r + 1]), make_float2(cl2, cl2),
+                                  make_float2(mu[r] == -INFINITY ? 0.f : -mu[r],
+                                              mu[r + 1] == -INFINITY ? 0.f : -mu[r + 1]));
+            const float a = ex2_approx(e.x), bq = ex2_approx(e.y);
             split_bf16x2(a, bq, h[q], l[q]);
             if constexpr (kRegL) {
-              lsum[r] += a;
-              lsum[r + 1] += bq;
+              const float2 s2 = add2(make_float2(lsum[r], lsum[r + 1]), make_float2(a, bq));
+              lsum[r] = s2.x;
+              lsum[r + 1] = s2.y;
             }
           }
           put_p(cc, h, l);
@@ -611,12 +614,13 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int r = 8 * cc + 2 * q;
-            const float a = ex2_approx(fmaf(x[r], cl2, -mu[r]));
-            const float bq = ex2_approx(fmaf(x[r + 1], cl2, -mu[r + 1]));
+            const float2 e = fma2(make_float2(x[r], x[r + 1]), make_float2(cl2, cl2), make_float2(-mu[r], -mu[r + 1]));
+            const float a = ex2_approx(e.x), bq = ex2_approx(e.y);
             split_bf16x2(a, bq, h[q], l[q]);
             if constexpr (kRegL) {
-              lsum[r] += a;
-              lsum[r + 1] += bq;
+              const float2 s2 = add2(make_float2(lsum[r], lsum[r + 1]), make_float2(a, bq));
+              lsum[r] = s2.x;
+              lsum[r + 1] = s2.y;
             }
           }
           put_p(cc, h, l);
