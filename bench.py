@@ -607,14 +607,14 @@ def rope_oracle_sample(B=4):
 _HEADERS = ['va_common.cuh', 'va_pipeline.cuh', 'va_tcgen05.cuh', 'va_kernels.h', 'va_rope_fused.cuh', 'va_merge.cuh']
 KERNEL_SOURCES = {"tc": ["va_attn_tc.cu"] + _HEADERS, "tck": ["va_attn_tck.cu"] + _HEADERS}
 PROFILED_TRAFFIC = {
-    "tree": {"sources": "tc", "sha256": "70c3e5370bd4bfe32946a381be3be85a5f4c2aded4ee0a821a09271d87644a4a",
-             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541208832},
-    "chain": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
-              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137794816},
-    "sparse": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
-               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141123584},
-    "paged": {"sources": "tck", "sha256": "3ac2bf0560619b0f83915e396c8c75aa547afe6e25040310866d230948464a69",
-              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470923264},
+    "tree": {"sources": "tc", "sha256": "dbe7d0513da0cf6bb631e91c5efa2f3355dd52787e658f0ad09e1a5a0889ad3e",
+             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541633536},
+    "chain": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
+              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137839616},
+    "sparse": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
+               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141137920},
+    "paged": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
+              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470995968},
 }
 
 
