@@ -56,6 +56,7 @@ constexpr int kIdxLoads = 16;         // score loads in flight per thread while 
 constexpr int kIdxBins = 2048;        // bins of one radix digit (11 bits)
 constexpr int kIdxCopies = 8;         // histogram copies, each shared by 4 warps
 constexpr int kIdxCandCap = (kIdxCopies - 1) * kIdxBins;  // candidate keys held behind one histogram
+constexpr int kIdxFastCap = 4096;     // candidates of the sampled-threshold select
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -123,17 +124,18 @@ __device__ __forceinline__ void hist_zero(const IdxSmem &sm) {
   for (int j = threadIdx.x; j < kIdxCopies * kIdxBins; j += kIdxThreads) sm.hist[j] = 0;
 }
 
-// The bucket of digit d that holds the kk-th largest counted key: thread t
-// owns the 1 or 2 bins just below bin 2047 - per * t (bins scanned from the
-// top).  Sets scratch[64] = bin, [65] = rank inside it, [66] = bucket taken whole.
-__device__ __forceinline__ void find_bucket(int d, int kk, const IdxSmem &sm, int copies) {
-  const int nb = 1 << digit_bits(d);
-  const int per = nb / kIdxThreads;  // 2 or 1
+// The bucket of a digit of `bits` bits (at most 11) that holds the kk-th
+// largest counted key: thread t owns the 1 or 2 bins just below bin
+// nb - 1 - per * t (bins scanned from the top).  Sets scratch[64] = bin,
+// [65] = rank inside it, [66] = bucket taken whole.
+__device__ __forceinline__ void find_bucket(int bits, int kk, const IdxSmem &sm, int copies) {
+  const int nb = 1 << bits;
+  const int per = nb > kIdxThreads ? nb / kIdxThreads : 1;  // 2 or 1
   const int tid = threadIdx.x;
   int c[2] = {0, 0};
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    if (j < per) {
+    if (j < per && tid * per + j < nb) {
       const int bin = nb - 1 - (tid * per + j);
       for (int h = 0; h < copies; ++h) c[j] += (int)sm.hist[h * kIdxBins + bin];
     }
@@ -247,7 +249,7 @@ __device__ Take select_top(const float *src, int L, int k, const IdxSmem &sm, co
       }
       __syncthreads();
     }
-    find_bucket(d, kk, sm, ncand >= 0 ? 1 : kIdxCopies);
+    find_bucket(bits, kk, sm, ncand >= 0 ? 1 : kIdxCopies);
     prefix |= (uint32_t)sm.scratch[64] << shift;
     pmask |= ((1u << bits) - 1u) << shift;
     kk = sm.scratch[65];
@@ -306,6 +308,212 @@ __device__ Take select_top(const float *src, int L, int k, const IdxSmem &sm, co
   return Take{0u, 0u, false};
 }
 
+// Mark in the bitmap every key of the key cache that a pending Take selects.
+__device__ void apply_take(const IdxSmem &sm, int L, const Take &t) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int base = 0; base < L; base += kIdxThreads) {
+    const int i = base + tid;
+    const bool take = i < L && take_key(sm.keys[i], t);
+    const uint32_t word = __ballot_sync(0xffffffffu, take);
+    if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
+  }
+  __syncthreads();
+}
+
+// Top k of src over the positions not yet in the bitmap, added to the bitmap,
+// in one pass over the scores where it can: a threshold from a sorted sample
+// of 1024 positions (chosen so that about 2 k eligible keys reach it), the
+// keys at or above it collected with their positions, and the radix select
+// run over those candidates only.  Every key of the top k is at or above the
+// threshold whenever at least k candidates reach it, so the result is exact.
+// Keys equal to the final threshold beyond the quota are taken in position
+// order (the tie rule).  Returns false -- having changed nothing -- when fewer
+// than k keys reach the sampled threshold, when a warp collects more than its
+// share of the candidate space, or when more than 32 keys tie at the final
+// threshold; select_top then does the work.
+constexpr int kIdxWarpCand = kIdxFastCap / (kIdxThreads / 32);  // candidate slots per warp
+__device__ bool select_top_fast(const float *src, int L, int k, const IdxSmem &sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto excluded = [&](int i) -> bool { return (sm.bitmap[i >> 5] >> (i & 31)) & 1u; };
+  uint32_t *ckey = sm.keys;                                      // [warp][kIdxWarpCand]
+  int *cpos = reinterpret_cast<int *>(sm.keys + kIdxFastCap);    // [warp][kIdxWarpCand]
+  int *wcount = sm.scratch + 72;                                 // [32]
+  uint32_t thr = 1u;  // the smallest counted key: every eligible key
+  const long long q = ((long long)k * 2048 + L - 1) / L + 8;  // sample rank of ~2 k keys
+  if (L > kIdxFastCap && q < kIdxThreads) {
+    // bitonic sort of the 1024 sample keys, largest first: exchanges between
+    // lanes by shuffles, between warps through two alternating arrays
+    const int ps = (int)(((long long)tid * L) >> 10);
+    uint32_t x = excluded(ps) ? 0u : order_key(__ldg(src + ps));
+    uint32_t *buf[2] = {sm.hist, sm.hist + kIdxThreads};
+    int pb = 0;
+    for (int kb = 2; kb <= kIdxThreads; kb <<= 1) {
+      for (int j = kb >> 1; j > 0; j >>= 1) {
+        uint32_t y;
+        if (j < 32) {
+          y = __shfl_xor_sync(0xffffffffu, x, j);
+        } else {
+          buf[pb][tid] = x;
+          __syncthreads();
+          y = buf[pb][tid ^ j];
+          pb ^= 1;
+        }
+        const bool keep_max = ((tid & kb) == 0) == ((tid & j) == 0);
+        x = keep_max ? max(x, y) : min(x, y);
+      }
+    }
+    if (tid == q - 1) sm.scratch[70] = (int)x;
+    __syncthreads();
+    thr = (uint32_t)sm.scratch[70];
+    __syncthreads();
+    if (thr == 0u) return false;
+  }
+  // one pass: the eligible keys at or above the threshold, with their
+  // positions, each warp into its own slots (no shared counter); four
+  // consecutive scores a load where the row is 16-byte aligned
+  int cw = 0;
+  uint32_t kmax = 0u;
+  uint32_t *wk = ckey + warp * kIdxWarpCand;
+  int *wp = cpos + warp * kIdxWarpCand;
+  // the float whose key is thr: !(f < thr_f) holds for every f whose key is
+  // at least thr (and for NaN, which the exact key test then settles)
+  const float thr_f = __uint_as_float((thr & 0x80000000u) ? (thr & 0x7fffffffu) : ~thr);
+  auto offer = [&](int i, float f) {
+    bool in = i < L && !(f < thr_f);
+    uint32_t key = 0u;
+    if (in) {
+      key = order_key(f);
+      in = key != 0u && key >= thr && !excluded(i);
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, in);
+    if (in) {
+      const int at = cw + __popc(m & ((1u << lane) - 1u));
+      kmax = max(kmax, key);
+      if (at < kIdxWarpCand) {
+        wk[at] = key;
+        wp[at] = i;
+      }
+    }
+    cw += __popc(m);
+  };
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    constexpr int kV = 8;  // float4 loads in flight per thread
+    for (int base = 0; base < L; base += kIdxThreads * 4 * kV) {
+      float4 v[kV];
+#pragma unroll
+      for (int u = 0; u < kV; ++u) {
+        const int i = base + 4 * (u * kIdxThreads + tid);
+        v[u] = i + 3 < L ? __ldg(reinterpret_cast<const float4 *>(src + i))
+                         : make_float4(i < L ? __ldg(src + i) : 0.f, i + 1 < L ? __ldg(src + i + 1) : 0.f,
+                                       i + 2 < L ? __ldg(src + i + 2) : 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kV; ++u) {
+        if (base + 4 * u * kIdxThreads >= L) break;  // uniform over the block
+        const int i = base + 4 * (u * kIdxThreads + tid);
+        offer(i, v[u].x);
+        offer(i + 1, v[u].y);
+        offer(i + 2, v[u].z);
+        offer(i + 3, v[u].w);
+      }
+    }
+  } else {
+    for (int base = 0; base < L; base += kIdxThreads * kIdxLoads) {
+      float v[kIdxLoads];
+#pragma unroll
+      for (int u = 0; u < kIdxLoads; ++u) {
+        const int i = base + u * kIdxThreads + tid;
+        v[u] = i < L ? __ldg(src + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kIdxLoads; ++u) {
+        if (base + u * kIdxThreads >= L) break;  // uniform over the block
+        offer(base + u * kIdxThreads + tid, v[u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  if (tid == 0) sm.scratch[71] = 0;
+  __syncthreads();
+  if (lane == 0) atomicMax(reinterpret_cast<unsigned *>(&sm.scratch[71]), kmax);
+  if (lane == 0) wcount[warp] = cw;
+  __syncthreads();
+  int n = 0;
+  bool over = false;
+#pragma unroll 4
+  for (int w = 0; w < kIdxThreads / 32; ++w) {
+    n += wcount[w];
+    over = over || wcount[w] > kIdxWarpCand;
+  }
+  if (over || n < k) return false;
+  // radix select among the candidates: every candidate lies in [thr, max],
+  // so the bits those two share are fixed and the digits (11 bits at a time)
+  // start below them, where the candidates differ
+  kmax = (uint32_t)sm.scratch[71];
+  const int common = kmax == thr ? 32 : __clz(kmax ^ thr);
+  uint32_t pmask = common == 0 ? 0u : (common == 32 ? 0xFFFFFFFFu : ~((1u << (32 - common)) - 1u));
+  uint32_t prefix = thr & pmask;
+  int kk = k;
+  bool exact = false;
+  int below = 32 - common;
+  if (below == 0) exact = n == k;  // every candidate equal
+  while (below > 0 && !exact) {
+    const int bits = below < 11 ? below : 11;
+    below -= bits;
+    const int shift = below;
+    for (int j = tid; j < kIdxBins; j += kIdxThreads) sm.hist[j] = 0;
+    __syncthreads();
+    for (int e = tid; e < kIdxFastCap; e += kIdxThreads) {
+      if ((e % kIdxWarpCand) >= wcount[e / kIdxWarpCand]) continue;
+      const uint32_t key = ckey[e];
+      if ((key & pmask) == prefix) atomicAdd(sm.hist + ((key >> shift) & ((1u << bits) - 1u)), 1u);
+    }
+    __syncthreads();
+    find_bucket(bits, kk, sm, 1);
+    prefix |= (uint32_t)sm.scratch[64] << shift;
+    pmask |= ((1u << bits) - 1u) << shift;
+    kk = sm.scratch[65];
+    exact = sm.scratch[66] != 0;
+    __syncthreads();
+  }
+  if (!exact) {
+    // keys equal to the full threshold (prefix) outnumber the kk still to
+    // take: the kk of them at the smallest positions (the tie rule); up to 32
+    // are ranked by one warp, more are left to select_top
+    if (tid == 0) sm.scratch[69] = 0;
+    __syncthreads();
+    int *tpos = reinterpret_cast<int *>(sm.hist);
+    for (int e = tid; e < kIdxFastCap; e += kIdxThreads) {
+      if ((e % kIdxWarpCand) >= wcount[e / kIdxWarpCand] || ckey[e] != prefix) continue;
+      const int at = atomicAdd(&sm.scratch[69], 1);
+      if (at < 32) tpos[at] = cpos[e];
+    }
+    __syncthreads();
+    const int ct = sm.scratch[69];
+    if (ct > 32) return false;
+    if (warp == 0) {
+      const int mine = lane < ct ? tpos[lane] : 0x7fffffff;
+      int rank = 0;
+#pragma unroll
+      for (int o = 0; o < 32; ++o) rank += __shfl_sync(0xffffffffu, mine, o) < mine ? 1 : 0;
+      if (lane < ct && rank < kk) atomicOr(&sm.bitmap[mine >> 5], 1u << (mine & 31));
+    }
+  }
+  // every key above the threshold bucket (and the bucket itself when it is
+  // taken whole)
+  for (int e = tid; e < kIdxFastCap; e += kIdxThreads) {
+    if ((e % kIdxWarpCand) >= wcount[e / kIdxWarpCand]) continue;
+    const uint32_t key = ckey[e] & pmask;
+    if (exact ? key >= prefix : key > prefix) {
+      const int i = cpos[e];
+      atomicOr(&sm.bitmap[i >> 5], 1u << (i & 31));
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
 struct IndexParams {
   int B, Hkv;
   const int32_t *seqlens;
@@ -359,18 +567,13 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   const int m1 = max(0, min(min(p.m_draft, room), ncand));
   const int m2 = max(0, min(room - m1, ncand - m1));
   const Take none{0u, 0u, false};
-  Take t = m1 > 0 ? select_top(p.sd + row * p.stride, L, m1, sm, none) : none;
-  if (m2 > 0) t = select_top(p.st + row * p.stride, L, m2, sm, t);
-  if (t.active) {
-    // the last pending take, from the key cache
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int base = 0; base < L; base += kIdxThreads) {
-      const int i = base + tid;
-      const bool take = i < L && take_key(sm.keys[i], t);
-      const uint32_t word = __ballot_sync(0xffffffffu, take);
-      if (lane == 0 && word != 0u) sm.bitmap[(base >> 5) + warp] |= word;
-    }
-    __syncthreads();
+  if (m1 > 0 && !select_top_fast(p.sd + row * p.stride, L, m1, sm)) {
+    const Take t = select_top(p.sd + row * p.stride, L, m1, sm, none);
+    if (t.active) apply_take(sm, L, t);
+  }
+  if (m2 > 0 && !select_top_fast(p.st + row * p.stride, L, m2, sm)) {
+    const Take t = select_top(p.st + row * p.stride, L, m2, sm, none);
+    if (t.active) apply_take(sm, L, t);
   }
 
   // bitmap -> ascending positions
