@@ -35,6 +35,16 @@ va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long 
  */
 va_status verify_attn_test_inject(unsigned long long wait_ns, int drop_part);
 
+/*
+ * Path of verify_build_index for the tests.  mode 0 (the default): each
+ * top-k selection first tries the one-pass sampled-threshold select and falls
+ * back to the radix select over all keys when the sample cannot decide;
+ * mode 1: the radix select over all keys only.  Both give the same sets; the
+ * tests compare each with the oracle.  Applies to every later launch of the
+ * process until called again.  Returns VA_ERR_INVALID_ARG for another mode.
+ */
+va_status verify_attn_test_index_path(int mode);
+
 #ifdef __cplusplus
 }
 #endif

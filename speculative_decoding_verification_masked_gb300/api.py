@@ -66,6 +66,7 @@ _SIGS = {
     "verify_attn_version": (ctypes.c_char_p, []),
     "verify_attn_selftest_wait_timeout": (_I, [_P, ctypes.c_ulonglong, _P]),
     "verify_attn_test_inject": (_I, [ctypes.c_ulonglong, _I]),
+    "verify_attn_test_index_path": (_I, [_I]),
     "verify_attn_dense_noalloc": (_I, [ctypes.POINTER(VaShape), _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 

@@ -63,6 +63,7 @@ uint64_t wait_limit_ns() {
 // next attention calls of the process.
 std::atomic<unsigned long long> g_test_wait_ns{0};
 std::atomic<int> g_test_drop_part{-1};
+std::atomic<int> g_test_index_radix{0};  // verify_attn_test_index_path
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -517,7 +518,7 @@ va_status verify_build_index(int B, int Hkv, const int32_t *seqlens, const float
   if (workspace != nullptr && !aligned(workspace, 256)) return fail(VA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   cudaError_t e = va::launch_build_index(B, Hkv, seqlens, score_draft, score_target, score_stride, n_sink, window,
                                          m_draft, budget, indices, n_indices, static_cast<int *>(workspace),
-                                         (cudaStream_t)stream);
+                                         g_test_index_radix.load() != 0, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "index launch");
   return ok();
 }
@@ -745,6 +746,12 @@ va_status verify_attn_test_inject(unsigned long long wait_ns, int drop_part) {
   if (wait_ns > 100000000ull) return fail(VA_ERR_INVALID_ARG, "wait_ns must be at most 0.1 s");
   g_test_wait_ns.store(wait_ns);
   g_test_drop_part.store(drop_part < 0 ? -1 : drop_part);
+  return ok();
+}
+
+va_status verify_attn_test_index_path(int mode) {
+  if (mode != 0 && mode != 1) return fail(VA_ERR_INVALID_ARG, "mode must be 0 or 1");
+  g_test_index_radix.store(mode);
   return ok();
 }
 

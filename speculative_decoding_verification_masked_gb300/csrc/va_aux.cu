@@ -521,6 +521,7 @@ struct IndexParams {
   int stride, n_sink, window, m_draft, budget;
   int32_t *indices, *n_indices;
   int *status;
+  int radix_only;  // skip the sampled-threshold select (test hook)
 };
 
 __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexParams p) {
@@ -567,11 +568,12 @@ __global__ void __launch_bounds__(kIdxThreads) build_index_kernel(const IndexPar
   const int m1 = max(0, min(min(p.m_draft, room), ncand));
   const int m2 = max(0, min(room - m1, ncand - m1));
   const Take none{0u, 0u, false};
-  if (m1 > 0 && !select_top_fast(p.sd + row * p.stride, L, m1, sm)) {
+  const bool fast = p.radix_only == 0;
+  if (m1 > 0 && !(fast && select_top_fast(p.sd + row * p.stride, L, m1, sm))) {
     const Take t = select_top(p.sd + row * p.stride, L, m1, sm, none);
     if (t.active) apply_take(sm, L, t);
   }
-  if (m2 > 0 && !select_top_fast(p.st + row * p.stride, L, m2, sm)) {
+  if (m2 > 0 && !(fast && select_top_fast(p.st + row * p.stride, L, m2, sm))) {
     const Take t = select_top(p.st + row * p.stride, L, m2, sm, none);
     if (t.active) apply_take(sm, L, t);
   }
@@ -604,7 +606,8 @@ size_t build_index_smem_bytes() {
 
 cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
                                const float *score_target, int score_stride, int n_sink, int window, int m_draft,
-                               int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream) {
+                               int budget, int32_t *indices, int32_t *n_indices, int *status, bool radix_only,
+                               cudaStream_t stream) {
   IndexParams p;
   p.B = B;
   p.Hkv = Hkv;
@@ -619,6 +622,7 @@ cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const flo
   p.indices = indices;
   p.n_indices = n_indices;
   p.status = status;
+  p.radix_only = radix_only ? 1 : 0;
   const size_t smem = build_index_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(build_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -77,7 +77,8 @@ cudaError_t launch_combine_generic(int n_rows, int n_parts, int D, const float *
 cudaError_t launch_tree_mask(int B, int T, const int32_t *parent, uint32_t *mask, int *status, cudaStream_t stream);
 cudaError_t launch_build_index(int B, int Hkv, const int32_t *seqlens, const float *score_draft,
                                const float *score_target, int score_stride, int n_sink, int window, int m_draft,
-                               int budget, int32_t *indices, int32_t *n_indices, int *status, cudaStream_t stream);
+                               int budget, int32_t *indices, int32_t *n_indices, int *status, bool radix_only,
+                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, uint64_t wait_ns, cudaStream_t stream);
 cudaError_t launch_validate_index(int B, int Hkv, const int32_t *seqlens, const int32_t *indices,
                                   const int32_t *n_indices, int max_indices, int len_cap, int T, int *status,

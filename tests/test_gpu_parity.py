@@ -319,8 +319,19 @@ def test_sparse_full_index_equals_dense_on_gpu():
 # verify index set (a5)
 # ----------------------------------------------------------------------------
 
+@pytest.fixture(params=["sampled", "radix"])
+def index_path(request):
+    """Runs a test with the builder's default path (the sampled-threshold
+    select, falling back to the radix select where the sample cannot decide)
+    and with the radix select over all keys only."""
+    L = va.api.lib()
+    assert L.verify_attn_test_index_path(1 if request.param == "radix" else 0) == 0
+    yield request.param
+    assert L.verify_attn_test_index_path(0) == 0
+
+
 @pytest.mark.parametrize("L_lo,L_hi", [(1, 300), (2000, 5000), (40000, 50000)])
-def test_build_index_bit_exact(L_lo, L_hi):
+def test_build_index_bit_exact(L_lo, L_hi, index_path):
     """Includes L below the budget, ties (coarse scores) and L past the shared-memory cache."""
     rng = np.random.default_rng(L_hi)
     B, Hkv = 4, 3
@@ -340,7 +351,7 @@ def test_build_index_bit_exact(L_lo, L_hi):
 
 @pytest.mark.parametrize("dist", ["normal", "negative", "wide", "few_distinct", "step"])
 @pytest.mark.parametrize("m_draft", [0, 300])
-def test_build_index_score_distributions(dist, m_draft):
+def test_build_index_score_distributions(dist, m_draft, index_path):
     """Score shapes that move the k-th key across the radix digits: signed and
     negative scores, a wide exponent range, a handful of distinct values (ties
     at every digit), and values spaced so bucket edges fall at the threshold."""
@@ -364,6 +375,35 @@ def test_build_index_score_distributions(dist, m_draft):
     sd = draw().astype(np.float32)
     st = draw().astype(np.float32)
     args = (4, 200, m_draft, 1500)
+    ref_idx, ref_n = oracle.build_verify_index(sd, st, seqlens, *args)
+    idx, n = va.verify_build_index(dev_i32(seqlens), torch.from_numpy(sd).cuda(), torch.from_numpy(st).cuda(), *args)
+    assert np.array_equal(n.cpu().numpy(), ref_n)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+@pytest.mark.parametrize("n_tied", [2, 5, 32, 33, 200])
+def test_build_index_ties_at_the_threshold(n_tied, index_path):
+    """Continuous scores with n_tied copies of the value at the k-th rank of
+    each select, spread over positions: the quota ends inside the tied run,
+    so the tie rule (lowest positions first) decides -- in the sampled path by
+    ranking up to 32 tied keys, beyond that by the radix select."""
+    rng = np.random.default_rng(n_tied)
+    B, Hkv = 2, 2
+    seqlens = np.array([24000, 17000], np.int32)
+    stride = int(seqlens.max())
+    sd = rng.random((B, Hkv, stride), dtype=np.float32)
+    st = rng.random((B, Hkv, stride), dtype=np.float32)
+    n_sink, window, m_draft, budget = 4, 256, 894, 2048
+    for b in range(B):
+        L = int(seqlens[b])
+        for h in range(Hkv):
+            for arr, k in ((sd, m_draft), (st, budget - n_sink - window - m_draft)):
+                row = arr[b, h, :L]
+                order = np.argsort(-row[n_sink:L - window], kind="stable") + n_sink
+                v = row[order[k - 1]]
+                pos = rng.choice(order[k:k + 4 * n_tied], size=n_tied - 1, replace=False)
+                row[pos] = v  # n_tied keys equal to the k-th largest
+    args = (n_sink, window, m_draft, budget)
     ref_idx, ref_n = oracle.build_verify_index(sd, st, seqlens, *args)
     idx, n = va.verify_build_index(dev_i32(seqlens), torch.from_numpy(sd).cuda(), torch.from_numpy(st).cuda(), *args)
     assert np.array_equal(n.cpu().numpy(), ref_n)
