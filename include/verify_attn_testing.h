@@ -27,8 +27,9 @@ va_status verify_attn_selftest_wait_timeout(void *workspace, unsigned long long 
  * tests.  Until called again, every later attention launch of the process
  * (a) uses wait_ns (0 < wait_ns <= 1e8) as the limit of each bounded device
  * wait instead of the default (wait_ns = 0 restores the default), and (b) if
- * drop_part >= 0, lets CTA number drop_part of the keys-on-lanes kernel skip
- * announcing the segment parts it computed, as if that message were lost:
+ * drop_part >= 0, lets CTA number drop_part of the tcgen05 attention kernels
+ * (the ones that merge split segments themselves) skip announcing the
+ * segment parts it computed, as if that message were lost:
  * the other parts of those segments then wait for it until the limit runs
  * out, record VA_ERR_TIMEOUT and finish without merging (drop_part < 0: off).
  * Nothing on the GPU faults or hangs; the call's outputs are undefined.
