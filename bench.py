@@ -419,6 +419,57 @@ def measure_scoring(va, peak, steps=256):
             "launches_per_call": 2, "cpu_baseline": oracle_rate(*scoring_oracle_sample(w))}
 
 
+def measure_sparse_overhead(va, scoring_us, steps=128):
+    """At the sparse workload's shape: the verification over the whole cache
+    (dense, every committed key) against the sparse path's parts -- the
+    verify-set build, the gathered attention -- and the importance pass
+    (timed by measure_scoring), each from CUDA events around graphs of 16
+    calls.  The full-cache call reads ~1.6 GB of K/V, far beyond L2; the index
+    build reads 25 MB of scores, which a serving step would also find in L2
+    right after the importance pass wrote them."""
+    w = W.make_workload("sparse", seed=0)
+    c = DeviceCase(w, va)
+    c.step()  # the verify sets, for the sparse-attention timing
+
+    def timed(fn):
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(16):
+                fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // 16)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (reps * 16)
+
+    full_us = timed(lambda: va.verify_attn_dense(c.q, c.k, c.v, c.seqlens, tree_parent=c.parent, tree_mask=c.mask,
+                                                 out=c.out, lse=c.lse, workspace=c.ws, scale=w.scale))
+    index_us = timed(lambda: va.verify_build_index(c.seqlens, c.sd, c.st, w.n_sink, w.window, w.m_draft, w.budget,
+                                                   indices=c.idx, n_indices=c.nidx, workspace=c.ws))
+    attn_us = timed(lambda: va.verify_attn_sparse(c.q, c.k, c.v, c.seqlens, c.idx, c.nidx, tree_parent=c.parent,
+                                                  tree_mask=c.mask, out=c.out, lse=c.lse, workspace=c.ws,
+                                                  scale=w.scale))
+    res = {"workload": f"sparse shape: B{w.B} T{w.T} Hq{w.Hq} Hkv{w.Hkv} d{w.D} bf16, prefixes 16K-32K, "
+                       f"verify sets of {w.budget}",
+           "full_cache_attention_us": round(full_us, 2), "index_build_us": round(index_us, 2),
+           "sparse_attention_us": round(attn_us, 2)}
+    if scoring_us is not None:
+        res["importance_pass_us"] = scoring_us
+        res["selection_overhead_frac_of_full_cache"] = round((index_us + scoring_us) / full_us, 4)
+        res["sparse_path_speedup_vs_full_cache"] = round(full_us / (index_us + scoring_us + attn_us), 3)
+    return res
+
+
 def e2e_measure(w, va, steps):
     """Through the public API with host buffers.  Every step copies its new
     inputs from pinned host memory to the device, runs the call, and copies out
@@ -986,6 +1037,8 @@ def main():
             others[name] = config_entry(r, world, peak)
     next_rows = measure_next_rows(va, peak) if args.all_configs and rank == 0 else None
     scoring = measure_scoring(va, peak) if args.all_configs and rank == 0 else None
+    sparse_overhead = (measure_sparse_overhead(va, scoring["us_per_call"] if scoring else None)
+                       if args.all_configs and rank == 0 else None)
     rope = measure_rope(va, peak) if args.all_configs and rank == 0 else None
     rope_fused = measure_rope_fused(va, peak) if args.all_configs and rank == 0 else None
     if rank != 0:
@@ -1023,6 +1076,8 @@ def main():
         line["after_verification"] = next_rows
     if scoring is not None:
         line["scoring_pass"] = scoring
+    if sparse_overhead is not None:
+        line["sparse_vs_full_cache"] = sparse_overhead
     if rope is not None:
         line["rope_draft"] = rope
     if rope_fused is not None:
