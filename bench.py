@@ -658,14 +658,14 @@ def rope_oracle_sample(B=4):
 _HEADERS = ['va_common.cuh', 'va_pipeline.cuh', 'va_tcgen05.cuh', 'va_kernels.h', 'va_rope_fused.cuh', 'va_merge.cuh']
 KERNEL_SOURCES = {"tc": ["va_attn_tc.cu"] + _HEADERS, "tck": ["va_attn_tck.cu"] + _HEADERS}
 PROFILED_TRAFFIC = {
-    "tree": {"sources": "tc", "sha256": "dbe7d0513da0cf6bb631e91c5efa2f3355dd52787e658f0ad09e1a5a0889ad3e",
-             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541633536},
-    "chain": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
-              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137839616},
-    "sparse": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
-               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141137920},
-    "paged": {"sources": "tck", "sha256": "29358bc38ae5404dc4d2311722d766fdd6c3a55eebce1506051779c0b4c5e6bf",
-              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470995968},
+    "tree": {"sources": "tc", "sha256": "53eb02e22ac33187e2da91687fb65e0fb462c1d8f9e5b28ef3c627de980938e0",
+             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541644544},
+    "chain": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
+              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137848064},
+    "sparse": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
+               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141196800},
+    "paged": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
+              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1471085312},
 }
 
 
