@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
     const uint64_t dV0 = umma_sdesc(smem_u32(stages) + Geo::kTileBytes, 8192, 1024);
     constexpr uint64_t kStageStep = Geo::kStageBytes >> 4;
     auto issue_s = [&](int i, int b, int st) {  // S_i(b) = Q_i K^T
-      if (!ok || lane != 0) return;
+      if (!ok) return;
       tc_fence_after();
       const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
       const uint32_t dS = tmem + 256 + 64 * (2 * i + b);
@@ -206,12 +206,12 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t qoff = (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
         const uint64_t koff = (uint64_t)(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
-        umma_ss(dS, dQ0 + (uint64_t)(i * (32768 >> 4)) + qoff, dK + koff, id_s, ks > 0 ? 1u : 0u);
+        umma_ss_warp(dS, dQ0 + (uint64_t)(i * (32768 >> 4)) + qoff, dK + koff, id_s, ks > 0 ? 1u : 0u);
       }
-      umma_commit(s_full + 2 * i + b);
+      umma_commit_warp(s_full + 2 * i + b);
     };
     auto issue_pv = [&](int i, int b, int st, bool first, bool exact) {  // O_i += P_i V
-      if (!ok || lane != 0) return;
+      if (!ok) return;
       tc_fence_after();
       const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
       const uint32_t aP = tmem + 256 + 64 * (2 * i + b);  // P hi; the residual 32 columns on
@@ -219,11 +219,11 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kTK / 16; ++kk) {
         const uint64_t bb = dV + (uint64_t)((kk * 2048) >> 4);
-        umma_ts(dO, aP + kk * 8, bb, id_o, (!first || kk > 0) ? 1u : 0u);
-        if (exact) umma_ts(dO, aP + 32 + kk * 8, bb, id_o, 1u);
+        umma_ts_warp(dO, aP + kk * 8, bb, id_o, (!first || kk > 0) ? 1u : 0u);
+        if (exact) umma_ts_warp(dO, aP + 32 + kk * 8, bb, id_o, 1u);
       }
-      umma_commit(o_done + 2 * i + b);
-      umma_commit(empty + st);  // this M-tile is done with the K/V stage once these complete
+      umma_commit_warp(o_done + 2 * i + b);
+      umma_commit_warp(empty + st);  // this M-tile is done with the K/V stage once these complete
     };
 
     for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
       }
     }
     // drain: every MMA the issuers started has finished before TMEM is released
-    if (lane == 0) umma_commit(drain);
+    umma_commit_warp(drain);
     mbar_wait(drain, 0u, p.wait_ns);
     tc_fence_before();
     named_bar_sync(kBarEnd, kSoftThreads + kMmaThreads);

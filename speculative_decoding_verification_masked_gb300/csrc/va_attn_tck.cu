@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (!ok || lane != 0) return;
+      if (!ok) return;
       tc_fence_after();
       const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
       const uint32_t dS = tmem + (2 + b) * NC;
@@ -330,12 +330,12 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t koff = (uint64_t)(((ks >> 2) * (TK * 128) + (ks & 3) * 32) >> 4);
         const uint64_t qoff = (uint64_t)(((ks >> 2) * (NR * 128) + (ks & 3) * 32) >> 4);
-        umma_ss(dS, dK + koff, dQ0 + qoff, id_s, ks > 0 ? 1u : 0u);
+        umma_ss_warp(dS, dK + koff, dQ0 + qoff, id_s, ks > 0 ? 1u : 0u);
       }
-      umma_commit(s_full + b);
+      umma_commit_warp(s_full + b);
     };
     auto issue_pv = [&](int st, int b, bool first) {  // [O_hi|O_lo]^T += V^T [P_hi|P_lo]^T
-      if (!ok || lane != 0) return;
+      if (!ok) return;
       tc_fence_after();
       const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
       const uint64_t dP = dP0 + (uint64_t)st * kStageStep;
@@ -344,11 +344,11 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       for (int kk = 0; kk < TK / 16; ++kk) {
         const uint64_t off = (uint64_t)((kk * 2048) >> 4);
         const uint32_t acc = kk > 0 ? 1u : acc0;
-        umma_ss(tO, dV + off, dP + off, id_o, acc);
-        if constexpr (!kRegL) umma_ts(tL, tOnes, dP + off, id_l, acc);
+        umma_ss_warp(tO, dV + off, dP + off, id_o, acc);
+        if constexpr (!kRegL) umma_ts_warp(tL, tOnes, dP + off, id_l, acc);
       }
-      umma_commit(o_done + b);
-      umma_commit(empty + st);  // the stage is free once these MMAs have read it
+      umma_commit_warp(o_done + b);
+      umma_commit_warp(empty + st);  // the stage is free once these MMAs have read it
     };
 
     for (int s = s0; s < p.S && tstart[s] < t1; ++s) {
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       }
     }
     // drain: every MMA issued has finished before TMEM is released
-    if (lane == 0) umma_commit(drain);
+    umma_commit_warp(drain);
     mbar_wait(drain, 0u, p.wait_ns);
     tc_fence_before();
     named_bar_sync(kBarEnd, kSoft + 32);
