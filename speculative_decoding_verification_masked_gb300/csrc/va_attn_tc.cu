@@ -23,7 +23,7 @@
 //                    1/16 of its row's final weight, and on spread-out rows
 //                    only a part's first tiles take the extra MMAs.
 //   warp 4*NMT       producer: TMA boxes (dense) / cp.async gathers (paged,
-//                    sparse) into a 3-stage ring (shared with the other kernel)
+//                    sparse) into a 4-stage ring (3 when shared memory is short)
 //   warps 4*NMT+1+i  PV issuer of M-tile i: O_i += P_i V (A = P from TMEM, B =
 //                    V as an MN-major operand).  Issuer 0 owns the TMEM
 //                    allocation.
@@ -52,19 +52,23 @@
 
 namespace va {
 
-constexpr int kTcStages = 3;
+// Stages of the K/V ring: 4 (measured on the tree workload: 3 stages 130.4 us,
+// 4 stages 125.5 us, 5 stages 128.6 us), or 3 when the plan's tile starts and
+// the rotary table leave no room for the fourth.
+constexpr int kTcStagesMin = 3;
+constexpr int kTcStagesMax = 4;
 
 // ---------------------------------------------------------------------------
 // shared memory plan
 // ---------------------------------------------------------------------------
-template <int NMT>
+template <int NMT, int NS>
 struct TcSmem {
   static constexpr int kQBytes = NMT * 2 * 128 * 128;  // NMT M-tiles x 2 columns x 128 rows x 128 B
   static constexpr int kStageBytes = StageGeom<__nv_bfloat16, 128>::kStageBytes;
   static constexpr int kStagesOff = kQBytes;
-  static constexpr int kBarOff = kStagesOff + kTcStages * kStageBytes;
+  static constexpr int kBarOff = kStagesOff + NS * kStageBytes;
   // barriers: full[NS], empty[NS], s_full[2][2], p_full[2][2], o_done[2][2], drain
-  static constexpr int kNumBars = 2 * kTcStages + 4 + 4 + 4 + 1;
+  static constexpr int kNumBars = 2 * NS + 4 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
   static constexpr int kLoFlagOff = kMiscOff + 16;          // int [2][2]: P residual written, per M-tile and buffer
   // then the rotary table of the segment (rope_table_bytes, 0 without
@@ -78,14 +82,13 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int NMT, bool kTma, bool kRope>
-__global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
+template <int NMT, bool kTma, bool kRope, int NS>
+__global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     verify_attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
-  using SM = TcSmem<NMT>;
+  using SM = TcSmem<NMT, NS>;
   using Geo = StageGeom<__nv_bfloat16, 128>;
   constexpr int D = 128;
-  constexpr int NS = kTcStages;
   constexpr int kSoftThreads = 128 * NMT;
   constexpr int kProducerWarp = 4 * NMT;
   constexpr int kMmaWarp0 = 4 * NMT + 1;  // PV issuer of M-tile i is warp kMmaWarp0 + i
@@ -553,28 +556,34 @@ __global__ void __launch_bounds__(TcSmem<NMT>::kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int NMT>
+template <int NMT, int NS>
 static size_t tc_smem_bytes(const AttnParams &p) {
-  return 1024 + (size_t)TcSmem<NMT>::kRopeOff + (size_t)rope_table_bytes(p) + (size_t)(p.S + 1) * 4;
+  return 1024 + (size_t)TcSmem<NMT, NS>::kRopeOff + (size_t)rope_table_bytes(p) + (size_t)(p.S + 1) * 4;
+}
+
+constexpr size_t kTcSmemLimit = 232448;  // bytes of dynamic shared memory a CTA may have
+
+// the ring depth an instance gets: the largest that fits the plan
+template <int NMT>
+static bool tc_deep_ring(const AttnParams &p) {
+  return tc_smem_bytes<NMT, kTcStagesMax>(p) <= kTcSmemLimit;
 }
 
 size_t attn_tc_smem_required(const AttnParams &p) {
-  return p.rows_pad > 128 ? tc_smem_bytes<2>(p) : tc_smem_bytes<1>(p);
+  return p.rows_pad > 128 ? tc_smem_bytes<2, kTcStagesMin>(p) : tc_smem_bytes<1, kTcStagesMin>(p);
 }
 
-template <int NMT, bool kTma>
-static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
-                               cudaStream_t stream) {
-  const size_t smem = tc_smem_bytes<NMT>(p);
-  // instances with and without the rotary embedding (code that never runs
-  // still costs the hot loop)
-  auto kern = p.positions != nullptr ? verify_attn_tc_kernel<NMT, kTma, true> : verify_attn_tc_kernel<NMT, kTma, false>;
+template <int NMT, bool kTma, bool kRope, int NS>
+static cudaError_t launch_tc_ns(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                                cudaStream_t stream) {
+  const size_t smem = tc_smem_bytes<NMT, NS>(p);
+  auto kern = verify_attn_tc_kernel<NMT, kTma, kRope, NS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // cooperative: every CTA is resident, so the wait for a segment's parts ends
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(TcSmem<NMT>::kThreads);
+  cfg.blockDim = dim3(TcSmem<NMT, NS>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -583,6 +592,20 @@ static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
+}
+
+// instances with and without the rotary embedding (code that never runs still
+// costs the hot loop), each with the deep ring or the minimum one
+template <int NMT, bool kTma>
+static cudaError_t launch_tc_t(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,
+                               cudaStream_t stream) {
+  if (p.positions != nullptr)
+    return tc_deep_ring<NMT>(p)
+               ? launch_tc_ns<NMT, kTma, true, kTcStagesMax>(p, tmk, tmv, grid, stream)
+               : launch_tc_ns<NMT, kTma, true, kTcStagesMin>(p, tmk, tmv, grid, stream);
+  return tc_deep_ring<NMT>(p)
+             ? launch_tc_ns<NMT, kTma, false, kTcStagesMax>(p, tmk, tmv, grid, stream)
+             : launch_tc_ns<NMT, kTma, false, kTcStagesMin>(p, tmk, tmv, grid, stream);
 }
 
 cudaError_t launch_attention_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv, int grid,

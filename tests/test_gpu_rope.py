@@ -273,6 +273,9 @@ FUSED_CASES = {
     "tc1_dense": ("tree", dict(B=2, Hkv=2, Hq=8, T=24, L=2600, depth=4), "parent", None),
     "tc2_dense": ("tree", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=3000), "parent", None),
     "tcp_dense": ("tree", dict(B=2, Hkv=2, Hq=8, L_lo=1500, L_hi=3000), "parent", ("VA_MANY_ROWS_KERNEL", "tcp")),
+    # 464 segments with the 32 KB rotary table: the rows-on-lanes kernel's
+    # shared memory holds only its 3-stage ring then
+    "tc2_short_ring": ("tree", dict(B=58, Hkv=8, Hq=32, L=1500), "parent", None),
     "tc1_paged16": ("paged", dict(B=2, Hkv=2, Hq=8, T=32, L_lo=1500, L_hi=2000, page_size=16, tree="depth", depth=5),
                     "parent", None),
     "tc2_sparse": ("sparse", dict(B=1, Hkv=2, Hq=8, T=40, L_lo=3000, L_hi=4000, budget=700, m_draft=200, window=64,
