@@ -313,38 +313,56 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
         rope_b = g.b;
       }
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-      for (int e = tid; e < NMT * 128 * 8; e += kSoftThreads) {
-        const int m = e / (128 * 8);
-        const int row = (e / 8) % 128;
-        const int ch = e % 8;
-        const int rr = g.rb * p.rows_pad + m * 128 + row;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      constexpr int kQIt = NMT * 128 * 8 / kSoftThreads;
+      uint4 lo[kQIt], hi[kQIt];
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {  // loads first: one round trip
+        const int e = tid + u * kSoftThreads;
+        const int rr = g.rb * p.rows_pad + (e / (128 * 8)) * 128 + (e / 8) % 128;
+        lo[u] = hi[u] = make_uint4(0, 0, 0, 0);
         if (rr < p.R) {
           const int t = rr / group;
           const int hq = g.hkv * group + rr % group;
           const uint4 *src = reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D);
-          lo = __ldg(src + ch);
-          hi = __ldg(src + ch + 8);
-          rope_rotate8_bf16(lo, hi, rope_tab + t * (D / 2) + ch * 8);
+          lo[u] = __ldg(src + e % 8);
+          hi[u] = __ldg(src + e % 8 + 8);
         }
-        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch)) = lo;
-        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch + 8)) = hi;
+      }
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoftThreads;
+        const int m = e / (128 * 8);
+        const int row = (e / 8) % 128;
+        const int ch = e % 8;
+        const int rr = g.rb * p.rows_pad + m * 128 + row;
+        if (rr < p.R) rope_rotate8_bf16(lo[u], hi[u], rope_tab + (rr / group) * (D / 2) + ch * 8);
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch)) = lo[u];
+        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch + 8)) = hi[u];
       }
       fence_proxy_async_smem();
     } else {
+      // every load of the thread in flight before the first store (one round
+      // trip, not one per row chunk)
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-      for (int e = tid; e < NMT * 128 * 16; e += kSoftThreads) {
+      constexpr int kQIt = NMT * 128 * 16 / kSoftThreads;
+      uint4 v[kQIt];
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoftThreads;
         const int m = e / (128 * 16);
         const int row = (e / 16) % 128;
-        const int ch = e % 16;
         const int rr = g.rb * p.rows_pad + m * 128 + row;
-        uint4 v = make_uint4(0, 0, 0, 0);
+        v[u] = make_uint4(0, 0, 0, 0);
         if (rr < p.R) {
           const int t = rr / group;
           const int hq = g.hkv * group + rr % group;
-          v = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + ch);
+          v[u] = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + e % 16);
         }
-        *reinterpret_cast<uint4 *>(sQ + m * 32768 + swz128(row, ch)) = v;
+      }
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoftThreads;
+        *reinterpret_cast<uint4 *>(sQ + (e / (128 * 16)) * 32768 + swz128((e / 16) % 128, e % 16)) = v[u];
       }
       fence_proxy_async_smem();
     }

@@ -418,32 +418,52 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
         rope_b = g.b;
       }
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-      for (int e = tid; e < NR * 8; e += kSoft) {
-        const int row = e >> 3, ch = e & 7;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        if (row < p.R) {
+      constexpr int kQIt = (NR * 8 + kSoft - 1) / kSoft;
+      uint4 lo[kQIt], hi[kQIt];
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {  // loads first: one round trip
+        const int e = tid + u * kSoft;
+        const int row = e >> 3;
+        lo[u] = hi[u] = make_uint4(0, 0, 0, 0);
+        if (e < NR * 8 && row < p.R) {
           const int t = row / group;
           const int hq = g.hkv * group + row % group;
           const uint4 *src = reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D);
-          lo = __ldg(src + ch);
-          hi = __ldg(src + ch + 8);
-          rope_rotate8_bf16(lo, hi, rope_tab + t * (D / 2) + ch * 8);
+          lo[u] = __ldg(src + (e & 7));
+          hi[u] = __ldg(src + (e & 7) + 8);
         }
-        *reinterpret_cast<uint4 *>(sQ + row * 128 + ((ch ^ (row & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4 *>(sQ + NR * 128 + row * 128 + ((ch ^ (row & 7)) << 4)) = hi;
+      }
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoft;
+        if (e >= NR * 8) continue;
+        const int row = e >> 3, ch = e & 7;
+        if (row < p.R) rope_rotate8_bf16(lo[u], hi[u], rope_tab + (row / group) * (D / 2) + ch * 8);
+        *reinterpret_cast<uint4 *>(sQ + row * 128 + ((ch ^ (row & 7)) << 4)) = lo[u];
+        *reinterpret_cast<uint4 *>(sQ + NR * 128 + row * 128 + ((ch ^ (row & 7)) << 4)) = hi[u];
       }
       fence_proxy_async_smem();
     } else {
+      // every load of the thread in flight before the first store
       const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-      for (int e = tid; e < NR * 16; e += kSoft) {
-        const int row = e >> 4, ch = e & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
+      constexpr int kQIt = NR * 16 / kSoft;
+      uint4 v[kQIt];
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoft;
+        const int row = e >> 4;
+        v[u] = make_uint4(0, 0, 0, 0);
         if (row < p.R) {
           const int t = row / group;
           const int hq = g.hkv * group + row % group;
-          v = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + ch);
+          v[u] = __ldg(reinterpret_cast<const uint4 *>(qb + (((size_t)g.b * p.T + t) * p.Hq + hq) * D) + (e & 15));
         }
-        *reinterpret_cast<uint4 *>(sQ + (ch >> 3) * (NR * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = v;
+      }
+#pragma unroll
+      for (int u = 0; u < kQIt; ++u) {
+        const int e = tid + u * kSoft;
+        const int row = e >> 4, ch = e & 15;
+        *reinterpret_cast<uint4 *>(sQ + (ch >> 3) * (NR * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) = v[u];
       }
       fence_proxy_async_smem();
     }
