@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
 
   if (warp == kProducerWarp) {
     bool pok = true;
-    produce_tiles<__nv_bfloat16, D, NS, kTK, NS, 1, kTma ? 1 : 0>(p, &tmk, &tmv, tstart, cr, stages, full, empty,
+    // at most NS-1 tiles in flight, and the second waits for the first: the
+    // first tile of every CTA lands sooner when the kernel starts (-1 us)
+    produce_tiles<__nv_bfloat16, D, NS, kTK, NS - 1, 1, kTma ? 1 : 0>(p, &tmk, &tmv, tstart, cr, stages, full, empty,
                                                                   abort_flag, use_tma, pok);
     // the merge grid may become resident once the last tiles are on their way
     // (it waits for this grid's completion before reading anything)
