@@ -134,10 +134,7 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     fence_mbar_init();
   }
   const CtaRange cr = plan_cta(p, tstart);  // contains __syncthreads
-  if (c >= cr.G) {
-    pdl_launch_dependents();
-    return;
-  }
+  if (c >= cr.G) return;
   const int t0 = cr.t0, t1 = cr.t1, s0 = cr.s0;
 
   if (warp == kProducerWarp) {
@@ -146,9 +143,6 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     // first tile of every CTA lands sooner when the kernel starts (-1 us)
     produce_tiles<__nv_bfloat16, D, NS, kTK, NS - 1, 1, kTma ? 1 : 0>(p, &tmk, &tmv, tstart, cr, stages, full, empty,
                                                                   abort_flag, use_tma, pok);
-    // the merge grid may become resident once the last tiles are on their way
-    // (it waits for this grid's completion before reading anything)
-    pdl_launch_dependents();
     return;
   }
 
