@@ -494,13 +494,14 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_nat = l > 0.f ? (m_used * cl2 + log2f(l)) * kLn2 : -INFINITY;
     const bool write = rvalid && ok;
+    const uint32_t wrows = __ballot_sync(0xffffffffu, write);  // rows of this warp that are written
 #pragma unroll
     for (int cch = 0; cch < 4; ++cch) {
       uint32_t u[32];
       tmem_ld32(tO + 32 * cch, u);
       tmem_ld_wait();
-      if (!write) continue;
       if (n_parts == 1) {
+        if (!write) continue;
         uint4 *ob = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                               (((size_t)g.b * p.T + t) * p.Hq + hq) * D + 32 * cch);
 #pragma unroll
@@ -513,12 +514,18 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
           ob[q4] = v;
         }
       } else {
-        float4 *op = reinterpret_cast<float4 *>(p.o_part +
-                                                ((size_t)(s + c) * p.rows_pad + mi * 128 + r) * D + 32 * cch);
+        // the warp's 32 rows through a 32 x 33 float tile in the Q buffer (its
+        // segment's S MMAs are all done): lane j then stores column j of each
+        // row, so every store writes 128 contiguous bytes of one row
+        float *tr = reinterpret_cast<float *>(sQ) + warp * (32 * 33);
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          op[q4] = make_float4(__uint_as_float(u[4 * q4]) * inv, __uint_as_float(u[4 * q4 + 1]) * inv,
-                               __uint_as_float(u[4 * q4 + 2]) * inv, __uint_as_float(u[4 * q4 + 3]) * inv);
+        for (int j = 0; j < 32; ++j) tr[lane * 33 + j] = __uint_as_float(u[j]) * inv;
+        __syncwarp();
+        float *op = p.o_part + ((size_t)(s + c) * p.rows_pad + mi * 128 + (warp & 3) * 32) * D + 32 * cch + lane;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if ((wrows >> i) & 1u) op[(size_t)i * D] = tr[i * 33 + lane];
+        __syncwarp();
       }
     }
     if (write) {
