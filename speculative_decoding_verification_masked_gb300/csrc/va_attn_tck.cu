@@ -317,8 +317,8 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       if (kRope && ok && lt * TK + TK > g.n_prefix) {
         // the draft keys of this tile, rotated in place before the MMA reads them
         const int r0 = max(0, g.n_prefix - lt * TK), r1 = min(TK, g.nkeys - lt * TK);
-        rope_rotate_tile_rows<__nv_bfloat16, D, TK>(stages + st * SM::kStageBytes, r0, r1, lt * TK + r0 - g.n_prefix,
-                                                    rope_tab, lane, 32);
+        rope_rotate_tile_rows_bf16_call<D, TK>(stages + st * SM::kStageBytes, r0, r1, lt * TK + r0 - g.n_prefix,
+                                               rope_tab, lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
       }

@@ -133,4 +133,13 @@ __device__ __forceinline__ void rope_rotate_tile_rows(uint8_t *tile, int r0, int
   }
 }
 
+// The same for bf16 tiles as an out-of-line call: a caller whose hot loop
+// would otherwise carry the rotation inline (the tcgen05 MMA issuer) keeps
+// that loop short.
+template <int D, int TK>
+__device__ __noinline__ void rope_rotate_tile_rows_bf16_call(uint8_t *tile, int r0, int r1, int t0, const float2 *tab,
+                                                            int tid, int nthreads) {
+  rope_rotate_tile_rows<__nv_bfloat16, D, TK>(tile, r0, r1, t0, tab, tid, nthreads);
+}
+
 }  // namespace va
