@@ -396,13 +396,10 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
       const int k0 = lt * kTK;
       const bool masked = k0 + kTK > g.n_prefix;
       if (masked) {
+        const uint64_t vis = tile_vis64(k0, g.n_prefix, g.nkeys, rmask);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int key = k0 + j;
-          bool vis = key < g.nkeys;
-          if (vis && key >= g.n_prefix) vis = (rmask >> (key - g.n_prefix)) & 1ull;
-          if (!vis) sv[j] = -INFINITY;
-        }
+        for (int j = 0; j < 64; ++j)
+          if (!((vis >> j) & 1ull)) sv[j] = -INFINITY;
       }
       float mx;
       {  // three-input maxima: 32 instructions, short dependency chains

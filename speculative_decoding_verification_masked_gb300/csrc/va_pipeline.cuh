@@ -208,6 +208,20 @@ __device__ __forceinline__ uint64_t draft_row(const AttnParams &p, int b, int t,
   return t >= 63 ? ~0ull : ((2ull << t) - 1);  // causal chain
 }
 
+// Visibility of the 64 keys k0 .. k0 + 63 for one row as a word: bit j is set
+// when key k0 + j exists (below nkeys) and is a prefix key or a draft key whose
+// bit the row's draft mask rmask has.  Built once per tile so that the
+// per-key tests are bit tests at fixed positions (a per-key shift by a
+// key-dependent amount kept the loop over the scores from being unrolled).
+__device__ __forceinline__ uint64_t tile_vis64(int k0, int n_prefix, int nkeys, uint64_t rmask) {
+  const int off = n_prefix - k0;  // position of the first draft key in the tile
+  uint64_t vis = off >= 64 ? ~0ull : (off <= 0 ? 0ull : (1ull << off) - 1ull);
+  if (off < 64) vis |= off >= 0 ? (rmask << off) : (-off >= 64 ? 0ull : rmask >> (-off));
+  const int nv = nkeys - k0;  // keys of the tile that exist
+  if (nv < 64) vis &= nv <= 0 ? 0ull : (1ull << nv) - 1ull;
+  return vis;
+}
+
 // ---------------------------------------------------------------------------
 // producer: one warp moves K/V rows of each tile with bulk copies
 // ---------------------------------------------------------------------------
