@@ -470,10 +470,35 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
     tc_fence_before();
     named_bar_arrive(kBarQ, kSoft + 32);
 
-    // ---- draft visibility: loads issued now, masks built before the first draft tile ----
+    // ---- draft visibility, when this part holds draft keys: per draft key
+    // dk, the packed rows r = t * group + h of the tokens t that see it.  Up to
+    // 32 rows it is built at once, while the part's first tiles are still on
+    // their way (chain -1%, sparse attention -3%); the 64-row instance, whose
+    // hot loop has no registers to spare, loads the parents now and builds the
+    // masks before the first draft tile ----
     DraftPre dpre{-1, -1, 0ull, 0ull};
-    if (warp == 0 && lt1 * TK > g.n_prefix) dpre = draft_prefetch(p, g.b);
+    const bool has_draft = lt1 * TK > g.n_prefix;
+    if (warp == 0 && has_draft) dpre = draft_prefetch(p, g.b);
     bool masks_ready = false;
+    auto build_masks = [&]() {
+      if (warp == 0) {
+        uint64_t lo, hi;
+        draft_rows(p, dpre, lo, hi);
+        if (lane < p.T) rowmask[lane] = lo;
+        if (lane + 32 < p.T) rowmask[lane + 32] = hi;
+      }
+      named_bar_sync(kBarSoft, kSoft);
+      if (tid < p.T) {
+        const uint64_t gbits = group >= 64 ? ~0ull : ((1ull << group) - 1);
+        uint64_t kmask = 0;
+        for (int t = 0; t < p.T; ++t)
+          if ((rowmask[t] >> tid) & 1ull) kmask |= gbits << (t * group);
+        keymask[tid] = kmask;
+      }
+      named_bar_sync(kBarSoft, kSoft);
+      masks_ready = true;
+    };
+    if (NR <= 32 && has_draft) build_masks();
 
     float mu[NR];  // reference max per row, log2 units
 #pragma unroll
@@ -490,25 +515,7 @@ __global__ void __launch_bounds__(TkCfg<NR, kTma>::kThreads, 1)
       const uint32_t tS = tO + (2 + b) * NC;
       const int key = lt * TK + tid;
       const bool masked = lt * TK + TK > g.n_prefix;
-      if (masked && !masks_ready) {
-        // per draft key dk, the packed rows r = t * group + h of the tokens t that see it
-        if (warp == 0) {
-          uint64_t lo, hi;
-          draft_rows(p, dpre, lo, hi);
-          if (lane < p.T) rowmask[lane] = lo;
-          if (lane + 32 < p.T) rowmask[lane + 32] = hi;
-        }
-        named_bar_sync(kBarSoft, kSoft);
-        if (tid < p.T) {
-          const uint64_t gbits = group >= 64 ? ~0ull : ((1ull << group) - 1);
-          uint64_t kmask = 0;
-          for (int t = 0; t < p.T; ++t)
-            if ((rowmask[t] >> tid) & 1ull) kmask |= gbits << (t * group);
-          keymask[tid] = kmask;
-        }
-        named_bar_sync(kBarSoft, kSoft);
-        masks_ready = true;
-      }
+      if (NR > 32 && masked && !masks_ready) build_masks();
       uint64_t km = ~0ull;  // rows that see this key
       if (masked) {
         if (key >= g.nkeys) km = 0;
