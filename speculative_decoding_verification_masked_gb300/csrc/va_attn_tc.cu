@@ -298,6 +298,12 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     const int n_parts = owner_cta(tstart[s + 1] - 1, cr.total, cr.G) - first_cta + 1;
     if (lt0 == 0 && tid == 0) p.meta[s] = make_int2(s + first_cta, n_parts);
 
+    // the draft structure of the part, when it holds draft keys (parents, or
+    // the mask words of tokens lane and lane + 32): loaded now, so that the
+    // round trip overlaps the one of Q
+    const bool has_draft = lt1 * kTK > g.n_prefix;
+    DraftPre dpre{-1, -1, 0ull, 0ull};
+    if (has_draft) dpre = draft_prefetch(p, g.b);
     // ---- Q of this segment into shared memory (both warpgroups) ----
     named_bar_sync(kBarSoft, kSoftThreads);  // previous segment's MMAs have all completed
     if constexpr (kRope) {
@@ -368,11 +374,12 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     const bool rvalid = rr < p.R;
     const int t = rvalid ? rr / group : 0;
     const int hq = g.hkv * group + (rvalid ? rr % group : 0);
-    uint64_t rmask = 0;
-    if (lt1 * kTK > g.n_prefix) {
-      uint64_t tl = 0, th = 0;
-      if (p.parent != nullptr) warp_tree_rows(p, g.b, tl, th);
-      rmask = draft_row(p, g.b, t, tl, th);
+    uint64_t rmask = 0;  // the draft keys this row sees
+    if (has_draft) {
+      uint64_t tl, th;
+      draft_rows(p, dpre, tl, th);
+      const uint64_t a = __shfl_sync(0xffffffffu, tl, t & 31), c2 = __shfl_sync(0xffffffffu, th, t & 31);
+      rmask = t < 32 ? a : c2;
     }
     float m_used = -INFINITY;  // reference max of the exponentials (raw score units)
     float l = 0.f;
