@@ -167,9 +167,13 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     const uint32_t id_o = umma_idesc(128, 128, 0, 1);
     int it = 0, jt = 0;
     bool ok = true;
+    // a phase already complete is taken at once; before spinning, a role
+    // checks whether another one has given up
     auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
-      if (ok && *abort_flag) ok = false;
-      if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
+      if (!ok || mbar_try_wait(bar, parity)) return;
+      if (*abort_flag) {
+        ok = false;
+      } else if (!mbar_wait(bar, parity, p.wait_ns)) {
         record_status(p.status, VA_ERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
         const int b = jt & 1;
         if (s_issuer) {
           // S(t) of each M-tile into buffer b once PV(t-2) has read P from it
+#pragma unroll
           for (int i = 0; i < NMT; ++i) {
             if (jt >= 2) wait_ok(o_done + 2 * i + b, (uint32_t)((jt - 2) >> 1) & 1u);
             if (i == 0) {
@@ -278,9 +283,11 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
   const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t tO = tmem + lane_bits + 128 * mi;
   bool ok = true;
-  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
-    if (ok && *abort_flag) ok = false;
-    if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {  // as the issuers'
+    if (!ok || mbar_try_wait(bar, parity)) return;
+    if (*abort_flag) {
+      ok = false;
+    } else if (!mbar_wait(bar, parity, p.wait_ns)) {
       record_status(p.status, VA_ERR_TIMEOUT);
       *abort_flag = 1;
       ok = false;
