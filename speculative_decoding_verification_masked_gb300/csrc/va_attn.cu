@@ -215,12 +215,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       for (int lt = lt0; lt < lt1; ++lt, ++it) {
         const int st = it % NS;
         const uint32_t ph = (uint32_t)(it / NS) & 1u;
-        if (ok && *abort_flag) ok = false;
-        if (ok && !mbar_wait(full + st, ph, p.wait_ns)) {
-          record_status(p.status, VA_ERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
-        }
+        role_wait(full + st, ph, ok, abort_flag, p.wait_ns, p.status);
         rotate_draft(lt, st);
         if (ok) {
           const uint32_t ks_addr = smem_u32(stages + st * C::kStageBytes);
@@ -460,12 +455,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       for (int lt = lt0; lt < lt1; ++lt, ++it) {
         const int st = it % NS;
         const uint32_t ph = (uint32_t)(it / NS) & 1u;
-        if (ok && *abort_flag) ok = false;
-        if (ok && !mbar_wait(full + st, ph, p.wait_ns)) {
-          record_status(p.status, VA_ERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
-        }
+        role_wait(full + st, ph, ok, abort_flag, p.wait_ns, p.status);
         rotate_draft(lt, st);
         if (ok) {
           const uint8_t *kt = stages + st * C::kStageBytes;

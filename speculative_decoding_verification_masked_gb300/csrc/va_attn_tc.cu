@@ -167,18 +167,7 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
     const uint32_t id_o = umma_idesc(128, 128, 0, 1);
     int it = 0, jt = 0;
     bool ok = true;
-    // a phase already complete is taken at once; before spinning, a role
-    // checks whether another one has given up
-    auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
-      if (!ok || mbar_try_wait(bar, parity)) return;
-      if (*abort_flag) {
-        ok = false;
-      } else if (!mbar_wait(bar, parity, p.wait_ns)) {
-        record_status(p.status, VA_ERR_TIMEOUT);
-        *abort_flag = 1;
-        ok = false;
-      }
-    };
+    auto wait_ok = [&](uint64_t *bar, uint32_t parity) { role_wait(bar, parity, ok, abort_flag, p.wait_ns, p.status); };
     // make stage `st` of tile lt ready for the MMAs: wait for it; on the dense
     // path zero the V rows past the segment end (TMA brought whole boxes)
     auto acquire_stage = [&](int st, uint32_t ph, int lt, const Seg &g) {
@@ -283,16 +272,7 @@ __global__ void __launch_bounds__(TcSmem<NMT, NS>::kThreads, 1)
   const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t tO = tmem + lane_bits + 128 * mi;
   bool ok = true;
-  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {  // as the issuers'
-    if (!ok || mbar_try_wait(bar, parity)) return;
-    if (*abort_flag) {
-      ok = false;
-    } else if (!mbar_wait(bar, parity, p.wait_ns)) {
-      record_status(p.status, VA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      ok = false;
-    }
-  };
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) { role_wait(bar, parity, ok, abort_flag, p.wait_ns, p.status); };
   int jt = 0;
   int rope_b = -1;  // sequence whose rotary table is in shared memory
   // split segments this CTA holds a part of (at most its first and its last)

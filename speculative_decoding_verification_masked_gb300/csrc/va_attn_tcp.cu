@@ -91,14 +91,7 @@ __device__ __forceinline__ void tp_produce(const AttnParams &p, const CUtensorMa
     prefetch_tmap(tmv);
   }
   bool ok = true;
-  auto wait_slot = [&](uint64_t *bar, uint32_t parity) {
-    if (ok && *abort_flag) ok = false;
-    if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
-      record_status(p.status, VA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      ok = false;
-    }
-  };
+  auto wait_slot = [&](uint64_t *bar, uint32_t parity) { role_wait(bar, parity, ok, abort_flag, p.wait_ns, p.status); };
   int it = 0;
   for (int s = cr.s0; s < p.S && tstart[s] < cr.t1; ++s) {
     const Seg g = seg_info(p, s, false);
@@ -234,14 +227,7 @@ __global__ void __launch_bounds__(TpSmem::kThreads, 1)
   const int group = p.Hq / p.Hkv;
 
   bool ok = true;
-  auto wait_ok = [&](uint64_t *bar, uint32_t parity) {
-    if (ok && *abort_flag) ok = false;
-    if (ok && !mbar_wait(bar, parity, p.wait_ns)) {
-      record_status(p.status, VA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      ok = false;
-    }
-  };
+  auto wait_ok = [&](uint64_t *bar, uint32_t parity) { role_wait(bar, parity, ok, abort_flag, p.wait_ns, p.status); };
 
   if (warp == kMmaWarp) {
     // ================================ MMA issuer ================================

@@ -115,6 +115,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   return true;
 }
 
+// Wait of a pipeline role that may have to give up: a phase already complete
+// is taken at once; otherwise the role first checks whether another role has
+// given up (abort_flag), then waits at most limit_ns, recording
+// VA_ERR_TIMEOUT and raising abort_flag when that runs out.  ok turns false
+// when the role stops waiting; a role with ok false waits for nothing.
+__device__ __forceinline__ void role_wait(uint64_t *bar, uint32_t parity, bool &ok, volatile int *abort_flag,
+                                          uint64_t limit_ns, int *status) {
+  if (!ok || mbar_try_wait(bar, parity)) return;
+  if (*abort_flag) {
+    ok = false;
+  } else if (!mbar_wait(bar, parity, limit_ns)) {
+    record_status(status, VA_ERR_TIMEOUT);
+    *abort_flag = 1;
+    ok = false;
+  }
+}
+
 // One tiled TMA box of a 3-D tensor map (coordinates innermost first) into
 // shared memory, completing its bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2, uint64_t *bar,

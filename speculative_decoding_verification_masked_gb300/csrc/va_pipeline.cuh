@@ -351,12 +351,7 @@ __device__ __forceinline__ int produce_tiles(const AttnParams &p, const CUtensor
     for (int lt = lt0; lt < lt1; ++lt, ++it) {
       const int st = it % NS;
       const uint32_t ph = (uint32_t)(it / NS) & 1u;
-      if (ok && *abort_flag) ok = false;
-      if (ok && !mbar_wait(empty + st, ph ^ 1u, p.wait_ns)) {
-        record_status(p.status, VA_ERR_TIMEOUT);
-        *abort_flag = 1;
-        ok = false;
-      }
+      role_wait(empty + st, ph ^ 1u, ok, abort_flag, p.wait_ns, p.status);
       // (with a cap, the second tile also waits for the first, which then lands sooner)
       const int gate = it >= MAXF ? it - MAXF : (it == 1 ? 0 : -1);
       if (MAXF < NS && ok && gate >= 0 &&
