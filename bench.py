@@ -658,14 +658,14 @@ def rope_oracle_sample(B=4):
 _HEADERS = ['va_common.cuh', 'va_pipeline.cuh', 'va_tcgen05.cuh', 'va_kernels.h', 'va_rope_fused.cuh', 'va_merge.cuh']
 KERNEL_SOURCES = {"tc": ["va_attn_tc.cu"] + _HEADERS, "tck": ["va_attn_tck.cu"] + _HEADERS}
 PROFILED_TRAFFIC = {
-    "tree": {"sources": "tc", "sha256": "53eb02e22ac33187e2da91687fb65e0fb462c1d8f9e5b28ef3c627de980938e0",
-             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541644544},
-    "chain": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
-              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 137848064},
-    "sparse": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
-               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141196800},
-    "paged": {"sources": "tck", "sha256": "b49305b4c7333f7460b21c39369385f20d5bdddf89b4452f87731e372829ca3a",
-              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1471085312},
+    "tree": {"sources": "tc", "sha256": "5f3eb81cd915d48d4d7ded3a3450edc49e011db4a13bdb337279b5b9734ee886",
+             "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541492736},
+    "chain": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+              "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 138061568},
+    "sparse": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+               "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141492480},
+    "paged": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+              "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470916864},
 }
 
 
