@@ -660,11 +660,11 @@ KERNEL_SOURCES = {"tc": ["va_attn_tc.cu"] + _HEADERS, "tck": ["va_attn_tck.cu"] 
 PROFILED_TRAFFIC = {
     "tree": {"sources": "tc", "sha256": "5f3eb81cd915d48d4d7ded3a3450edc49e011db4a13bdb337279b5b9734ee886",
              "kernel": "verify_attn_tc_kernel<2, TMA>", "bytes": 541492736},
-    "chain": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+    "chain": {"sources": "tck", "sha256": "82f27a4640fe712ccc1c3bc4dc5d7408724acaa1eecde6bd4dd2565ec887c29c",
               "kernel": "verify_attn_tck_kernel<32, TMA>", "bytes": 138061568},
-    "sparse": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+    "sparse": {"sources": "tck", "sha256": "82f27a4640fe712ccc1c3bc4dc5d7408724acaa1eecde6bd4dd2565ec887c29c",
                "kernel": "verify_attn_tck_kernel<32, gather>", "bytes": 141492480},
-    "paged": {"sources": "tck", "sha256": "9006ecb68d459f01187aa12897b4736159f9bb528aed31b798d8517b0928a021",
+    "paged": {"sources": "tck", "sha256": "82f27a4640fe712ccc1c3bc4dc5d7408724acaa1eecde6bd4dd2565ec887c29c",
               "kernel": "verify_attn_tck_kernel<64, TMA>", "bytes": 1470916864},
 }
 

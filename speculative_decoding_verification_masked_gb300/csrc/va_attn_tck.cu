@@ -19,7 +19,8 @@
 // bf16 output rounding, at no extra MMA: an MMA of N <= 128 costs the same
 // issue time as one of half that width.
 //
-// Roles (6 warps, one CTA per SM):
+// Roles (6 warps, 7 when a second producer warp shares a gather; one CTA per
+// SM, cooperative launch):
 //   warps 0-3  softmax: thread k owns key k of the tile (TMEM lane k) and all
 //              NR rows of it.  Scores are taken in log2 units against a
 //              per-row reference max that moves only when some score of the
@@ -30,8 +31,9 @@
 //              P (bf16 hi and lo parts) is written as the MN-major P^T
 //              operand over the K tile of the same stage, which the S MMA has
 //              finished reading.  In the epilogue thread d owns output column d.
-//   warp 4     producer: TMA boxes (dense) or cp.async gathers (paged, sparse)
-//              into a 3-stage ring of 128-key K and V tiles (64 KB a stage)
+//   warp 4     producer: TMA boxes (dense, paged with pages of 8 rows or more)
+//              or cp.async gathers (sparse, small pages) into a 3-stage ring
+//              of 128-key K and V tiles (64 KB a stage)
 //   warp 5     MMA issuer and TMEM owner: S of tile i+2 is issued as soon as
 //              the softmax of tile i has released its S buffer.
 // TMEM columns (NC = max(NR, 32)): O^T hi at 0 and lo at NR, S buffers at 2NC
